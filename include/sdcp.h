@@ -1,0 +1,198 @@
+/*
+ * sdcp.h - C ABI of libsdcp, the batched acceptance step of a speculative-decoding
+ * verifier, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the verifier's "Acceptance" step of the Speculative Decoding
+ * Coordination Protocol (IETF draft-li-mlc-inference-acceleration-00, "Speculative
+ * Decoding Coordination Protocol (SDCP) for Distributed Inference with Multi-Level
+ * Caches"):
+ *   - the sampling profile of Section 4.1 (temperature, then top-k, then top-p; a
+ *     temperature of zero selects the most probable token, ties to the smallest id)
+ *     turns logits into the distributions p (target) and q (draft);
+ *   - Section 6.4, Rule 1 (greedy) and Rule 2 (speculative sampling) decide how many
+ *     of the M proposed tokens are accepted and which one additional token is emitted;
+ *   - Section 6.3, "Preconditions of the rule": q[i](x[i]) must be non-zero at every
+ *     proposed position before any random value is drawn;
+ *   - Section 6.3, "Scoring": the verifier may batch the proposals of many sessions;
+ *   - Section 5.2, "verdict": the results are the accepted count a (0 <= a <= M) and
+ *     the emitted tokens;
+ *   - Table 2 (Section 6.9), problem types: a per-session status mirrors the ones that
+ *     can arise inside this call.
+ *
+ * Random values are Philox4x32-10 uniforms (Salmon, Moraes, Dror and Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC'11), keyed by the session's
+ * 64-bit seed (key word 0 = low 32 bits, key word 1 = high 32 bits), with counter
+ * (position, purpose, round, session_tag); purpose 0 is the acceptance test and 1 the
+ * additional token, as in SDCP Section 6.4.  The uniform is
+ * ((w0 << 21) | (w1 >> 11)) * 2^-53, the first 53 bits of the output, like the
+ * 53-bit value of Section 6.4.
+ *
+ * Ragged batch layout (all device memory, row-major, row stride V elements):
+ *   B sessions; session b proposes M_b = m_offsets[b+1] - m_offsets[b] tokens.
+ *   target row of session b at position i (i = 0..M_b):  T[m_offsets[b] + b + i]
+ *   draft row of session b at position i (i = 0..M_b-1): D[m_offsets[b] + i]
+ *   draft token of session b at position i:               draft_tokens[m_offsets[b] + i]
+ *   output tokens of session b:                           out_tokens[m_offsets[b] + b + j],
+ *                                                         j = 0..n_out[b]-1; the slots
+ *                                                         j = n_out[b]..M_b hold -1.
+ *
+ * Ownership: the caller owns every buffer and the stream.  The library allocates
+ * nothing, never synchronises the stream and keeps no state between calls, so calls on
+ * different streams with different workspaces may run concurrently.  Results are a
+ * pure function of the inputs: re-running a call reproduces every output bit for bit.
+ *
+ * Errors: a non-zero return code (SDCP_E_*) means nothing was launched (argument
+ * errors) or a launch failed (SDCP_E_LAUNCH).  Errors that depend on values stored in
+ * device memory are reported per session in status[] (SDCP_S_*); such a session gets
+ * accepted = 0, n_out = 0 and all its output slots -1, and so commits nothing.
+ */
+#ifndef SDCP_H
+#define SDCP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- element types of the logits ------------------------------------------------ */
+#define SDCP_F32  0   /* IEEE binary32 */
+#define SDCP_BF16 1   /* bfloat16 (upper half of a binary32) */
+
+/* ---- acceptance rules: SDCP Section 10.2.2 registry ------------------------------ */
+#define SDCP_RULE_GREEDY 1              /* Rule 1 */
+#define SDCP_RULE_SPECULATIVE_SAMPLING 2 /* Rule 2 */
+
+/* ---- return codes ---------------------------------------------------------------- */
+#define SDCP_OK           0
+#define SDCP_E_INVALID    1  /* null pointer, B < 0, V < 1, unknown dtype, sizes overflow */
+#define SDCP_E_WORKSPACE  2  /* workspace null, too small or not 256-byte aligned */
+#define SDCP_E_ALIGN      3  /* a logits pointer is not aligned to its element size */
+#define SDCP_E_TOO_LARGE  4  /* V above SDCP_MAX_VOCAB or a row count above INT32_MAX */
+#define SDCP_E_LAUNCH     5  /* a CUDA launch failed (cudaGetLastError after launch) */
+#define SDCP_E_DEVICE     6  /* no usable CUDA device / device query failed */
+
+/* ---- per-session status (mirrors SDCP Table 2 problem types) ---------------------- */
+#define SDCP_S_OK             0
+#define SDCP_S_BAD_PROPOSAL   1  /* "sdcp-bad-proposal": a token outside [0,V), or, under
+                                    Rule 2, q[i](x[i]) = 0 at some position (Section 6.4) */
+#define SDCP_S_LIMIT          2  /* "sdcp-limit": M outside [1, SDCP_MAX_M] (m_max <= 64,
+                                    Section 4.1; 1 <= M, Section 6.2) */
+#define SDCP_S_BAD_PARAMS     3  /* unknown rule id, top_p_milli > 1000, inconsistent
+                                    m_offsets, or a scored row holding NaN, +inf or only
+                                    -inf (no distribution can be formed) */
+#define SDCP_S_Q_UNAVAILABLE  4  /* "sdcp-q-unavailable": Rule 2 without draft logits */
+
+#define SDCP_MAX_M      64          /* m_max upper bound, SDCP Section 4.1 contract */
+#define SDCP_MAX_VOCAB  (1 << 24)   /* ids and ranks are int32; 16 Mi keeps all sums exact */
+
+/* One per session, device memory, 32 bytes, naturally aligned. */
+typedef struct sdcp_session_params {
+  uint32_t rule_id;           /* SDCP_RULE_*; anything else -> SDCP_S_BAD_PARAMS */
+  uint32_t temperature_milli; /* temperature x 1000 (Section 4.1); 0 selects the argmax */
+  uint32_t top_k;             /* keep the top_k most probable; 0 or >= V disables */
+  uint32_t top_p_milli;       /* nucleus mass x 1000, <= 1000; 1000 disables */
+  uint64_t seed;              /* Philox key of the verifier's random values */
+  uint32_t round;             /* protocol round of this proposal */
+  uint32_t session_tag;       /* 32 bits that name the session (e.g. the first four
+                                 octets of its 16-octet identifier), not the batch slot */
+} sdcp_session_params;
+
+/*
+ * Bytes of device workspace sdcp_verify_batch and sdcp_row_stats need for a batch of
+ * B sessions with total_drafts = sum of M_b proposed tokens.  Returns 0 for invalid
+ * sizes (B < 0, total_drafts < 0, V < 1 or V > SDCP_MAX_VOCAB).
+ */
+size_t sdcp_workspace_bytes(int64_t V, int32_t B, int64_t total_drafts);
+
+/*
+ * Verify one ragged batch (SDCP Sections 4.1, 6.3 and 6.4).
+ *
+ * target_logits  device, [total_drafts + B][V] of dtype; the scores p[1..M+1] of each
+ *                session (Section 6.3 "Scoring"), laid out as described above.
+ * draft_logits   device, [total_drafts][V] of dtype, or NULL when no session uses Rule 2
+ *                (a Rule 2 session then gets SDCP_S_Q_UNAVAILABLE).  Rows of Rule 1
+ *                sessions are never read.  The profile of the session is applied to these
+ *                logits to form q (the draft distribution the tokens were sampled from).
+ * dtype          SDCP_F32 or SDCP_BF16, for both logits arrays.
+ * V              vocabulary size, 1..SDCP_MAX_VOCAB.  Any V is accepted; rows whose start
+ *                is not 16-byte aligned are read with narrower loads at their ends.
+ * B              number of sessions, >= 0 (B = 0 launches nothing).
+ * m_offsets      device, [B+1] int32, m_offsets[0] = 0, non-decreasing,
+ *                m_offsets[B] = total_drafts; inconsistent values give SDCP_S_BAD_PARAMS
+ *                to the sessions they touch, never an out-of-range access.
+ * total_drafts   host copy of m_offsets[B] (sizes the launch without a device read).
+ * draft_tokens   device, [total_drafts] int32, the proposed tokens x[i].
+ * params         device, [B] sdcp_session_params.
+ * accepted       device out, [B] int32: a, the number of accepted draft tokens.
+ * n_out          device out, [B] int32: a + 1 emitted tokens (0 for a failed session).
+ * out_tokens     device out, [total_drafts + B] int32 (layout above).
+ * status         device out, [B] int32 SDCP_S_*.
+ * workspace      device scratch of at least sdcp_workspace_bytes(V, B, total_drafts)
+ *                bytes, 256-byte aligned; its contents need no initialisation and are
+ *                garbage afterwards.
+ * stream         the cudaStream_t (as void*) all work is enqueued on; NULL = legacy stream.
+ *
+ * Returns SDCP_OK or SDCP_E_*.  Asynchronous: results are ready when the stream reaches
+ * this point.
+ */
+int sdcp_verify_batch(const void* target_logits, const void* draft_logits, int dtype,
+                      int64_t V, int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                      const int32_t* draft_tokens, const sdcp_session_params* params,
+                      int32_t* accepted, int32_t* n_out, int32_t* out_tokens,
+                      int32_t* status, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
+ * Per-row statistics of the sampling profile (parity hook for the first phase).
+ *
+ * Same inputs as sdcp_verify_batch.  For every target row r (0 <= r < total_drafts + B)
+ * and then every draft row (total_drafts of them) it writes one sdcp_row_stat to
+ * stats_out (device, [2 * total_drafts + B]), target rows first.  All rows are given the
+ * full statistics regardless of the session's rule (draft rows of a session with an
+ * invalid rule or M get flags = SDCP_ROW_SKIPPED).  Row statistics follow Section 4.1:
+ *   lmax    the largest logit of the row (before temperature);
+ *   log_s   natural log of S = sum over the kept set of exp((l_j - lmax) * 1000/T);
+ *   lp_x    natural log of the probability of the row's draft token x (target row i < M
+ *           and draft row i carry x[i]); -inf when x is outside the kept set or its
+ *           logit is -inf; NaN for rows without a draft token (target row M) or x out
+ *           of range;
+ *   argmax  smallest id among the largest logits;
+ *   kept    number of tokens in the kept set (1 when the temperature is 0);
+ *   flags   SDCP_ROW_* bits.
+ */
+typedef struct sdcp_row_stat {
+  float lmax;
+  float log_s;
+  float lp_x;
+  int32_t argmax;
+  int32_t kept;
+  uint32_t thr_key;   /* internal: order key of the last kept token */
+  int32_t thr_id;     /* internal: id bound among tokens sharing that key */
+  uint32_t flags;
+} sdcp_row_stat;
+
+#define SDCP_ROW_INVALID   1u  /* NaN, +inf, or no finite logit: no distribution */
+#define SDCP_ROW_X_KEPT    2u  /* the draft token is in the kept set with a finite logit */
+#define SDCP_ROW_SKIPPED   4u  /* row not processed */
+#define SDCP_ROW_FALLBACK  8u  /* the threshold needed the generic multi-pass search */
+
+int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtype,
+                   int64_t V, int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                   const int32_t* draft_tokens, const sdcp_session_params* params,
+                   sdcp_row_stat* stats_out, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/* Human-readable text for an SDCP_E_* code (static storage, never NULL). */
+const char* sdcp_strerror(int code);
+
+/* ABI version of this header; bumps on any incompatible change. */
+#define SDCP_ABI_VERSION 1
+int sdcp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDCP_H */

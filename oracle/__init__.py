@@ -1,0 +1,178 @@
+"""CPU oracle of the SDCP verifier's acceptance step (test infrastructure).
+
+The oracle is the plain fp64 C program in ``sdcp_oracle.c`` (see its header for the
+definitions it follows: the sampling profile of SDCP Section 4.1, the precondition of
+Section 6.3 and Rules 1 and 2 of Section 6.4 of the SDCP draft
+draft-li-mlc-inference-acceleration-00).  This module only builds it with gcc and
+marshals numpy arrays into it.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its ``cpu_baseline`` leg and
+its ``--impl reference`` arm) may import this package.  It shares no code with the CUDA
+path and imports nothing from it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sdcp_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libsdcp_oracle.so")
+
+F32, BF16 = 0, 1
+S_OK, S_BAD_PROPOSAL, S_LIMIT, S_BAD_PARAMS, S_Q_UNAVAILABLE = 0, 1, 2, 3, 4
+MMAX = 64
+
+# Same 32-byte layout as one session's parameters in the C ABI (rule, temperature x1000,
+# top_k, top_p x1000, seed, round, session tag).
+PARAMS_DTYPE = np.dtype([("rule_id", "<u4"), ("temperature_milli", "<u4"), ("top_k", "<u4"),
+                         ("top_p_milli", "<u4"), ("seed", "<u8"), ("round", "<u4"),
+                         ("session_tag", "<u4")])
+
+
+class RowInfo(ctypes.Structure):
+    _fields_ = [("lmax", ctypes.c_double), ("log_s", ctypes.c_double),
+                ("argmax", ctypes.c_int32), ("kept", ctypes.c_int32), ("k1", ctypes.c_int32),
+                ("invalid", ctypes.c_int32), ("topp_cum_before", ctypes.c_double),
+                ("topp_cum_at", ctypes.c_double), ("topp_target", ctypes.c_double)]
+
+
+DETAIL_DTYPE = np.dtype([
+    ("status", "<i4"), ("a", "<i4"), ("n_out", "<i4"), ("extra_mode", "<i4"),
+    ("extra_token", "<i4"), ("extra_pos", "<i4"), ("m", "<i4"), ("pad", "<i4"),
+    ("u1", "<f8"), ("W", "<f8"), ("c_lo", "<f8"), ("c_hi", "<f8"),
+    ("u0", "<f8", (MMAX,)), ("ratio", "<f8", (MMAX,)), ("log_p", "<f8", (MMAX,)),
+    ("log_q", "<f8", (MMAX,)), ("topp_margin", "<f8")])
+
+EXTRA_ARGMAX, EXTRA_RESIDUAL, EXTRA_BONUS, EXTRA_RESIDUAL_AS_P = 1, 2, 3, 4
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc, OpenMP, -O2, no -ffast-math) in place; return its path."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i64, i32, u32, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint64
+        L.oracle_philox4x32_10.argtypes = [vp, vp, vp]
+        L.oracle_philox4x32_10.restype = None
+        L.oracle_uniform.argtypes = [u64, u32, u32, u32, u32]
+        L.oracle_uniform.restype = ctypes.c_double
+        L.oracle_row_dist.argtypes = [vp, ctypes.c_int, i64, u32, u32, u32, vp, vp, ctypes.POINTER(RowInfo)]
+        L.oracle_row_dist.restype = ctypes.c_int
+        L.oracle_draw_cdf.argtypes = [vp, vp, i64, vp]
+        L.oracle_draw_cdf.restype = ctypes.c_double
+        L.oracle_draw.argtypes = [vp, vp, i64, ctypes.c_double]
+        L.oracle_draw.restype = ctypes.c_int32
+        L.oracle_verify_batch.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp,
+                                          vp, vp, vp, vp, vp, ctypes.c_int]
+        L.oracle_verify_batch.restype = ctypes.c_int
+        L.oracle_max_threads.argtypes = []
+        L.oracle_max_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(arr: np.ndarray) -> int:
+    """float32 arrays are binary32 logits; uint16 arrays hold raw bfloat16 bits."""
+    if arr.dtype == np.float32:
+        return F32
+    if arr.dtype == np.uint16:
+        return BF16
+    raise TypeError("logits must be float32 or uint16 (raw bfloat16 bits), got %s" % arr.dtype)
+
+
+def philox4x32_10(counter, key):
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.zeros(4, dtype=np.uint32)
+    lib().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed: int, round_: int, position: int, purpose: int, tag: int) -> float:
+    return lib().oracle_uniform(seed, round_, position, purpose, tag)
+
+
+def row_dist(row: np.ndarray, temperature_milli: int = 1000, top_k: int = 0,
+             top_p_milli: int = 1000, want_dist: bool = True, want_kept: bool = False):
+    """The sampling profile of SDCP Section 4.1 on one row.  Returns (dist, kept, info, rc)."""
+    row = np.ascontiguousarray(row)
+    V = row.shape[0]
+    dist = np.zeros(V, dtype=np.float64) if want_dist else None
+    kept = np.zeros(V, dtype=np.uint8) if want_kept else None
+    info = RowInfo()
+    rc = lib().oracle_row_dist(_ptr(row), _dtype_code(row), V, temperature_milli, top_k,
+                               top_p_milli, _ptr(dist), _ptr(kept), ctypes.byref(info))
+    return dist, kept, info, rc
+
+
+def draw_cdf(p: np.ndarray, q: np.ndarray | None = None):
+    """Cumulative weights of a draw, ids ascending (residual max(0,p-q) if q is given)."""
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    q = None if q is None else np.ascontiguousarray(q, dtype=np.float64)
+    C = np.zeros_like(p)
+    W = lib().oracle_draw_cdf(_ptr(p), _ptr(q), p.shape[0], _ptr(C))
+    return C, W
+
+
+def draw(p: np.ndarray, q: np.ndarray | None, u: float) -> int:
+    """Inverse-CDF draw of the additional token for one uniform u."""
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    q = None if q is None else np.ascontiguousarray(q, dtype=np.float64)
+    return int(lib().oracle_draw(_ptr(p), _ptr(q), p.shape[0], float(u)))
+
+
+def verify_batch(target: np.ndarray, draft: np.ndarray | None, m_offsets: np.ndarray,
+                 draft_tokens: np.ndarray, params: np.ndarray, nthreads: int = 1,
+                 want_detail: bool = True):
+    """Rules 1 and 2 of SDCP Section 6.4 over a ragged batch (layout of the C ABI).
+
+    target: [total_drafts + B, V], draft: [total_drafts, V] or None (float32 or raw bf16
+    bits as uint16).  Returns a dict of numpy arrays (accepted, n_out, out_tokens, status,
+    detail).
+    """
+    target = np.ascontiguousarray(target)
+    dcode = _dtype_code(target)
+    if draft is not None:
+        draft = np.ascontiguousarray(draft)
+        if draft.dtype != target.dtype:
+            raise TypeError("target and draft logits must share a dtype")
+    m_offsets = np.ascontiguousarray(m_offsets, dtype=np.int32)
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    params = np.ascontiguousarray(params, dtype=PARAMS_DTYPE)
+    B = params.shape[0]
+    V = target.shape[1]
+    total = int(draft_tokens.shape[0])
+    acc = np.zeros(B, np.int32)
+    nout = np.zeros(B, np.int32)
+    toks = np.full(total + B, -1, np.int32)
+    st = np.zeros(B, np.int32)
+    det = np.zeros(B, DETAIL_DTYPE) if want_detail else None
+    rc = lib().oracle_verify_batch(_ptr(target), _ptr(draft), dcode, V, B, _ptr(m_offsets),
+                                   total, _ptr(draft_tokens), _ptr(params), _ptr(acc),
+                                   _ptr(nout), _ptr(toks), _ptr(st), _ptr(det), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_verify_batch rejected its arguments (rc=%d)" % rc)
+    return {"accepted": acc, "n_out": nout, "out_tokens": toks, "status": st, "detail": det}
+
+
+def max_threads() -> int:
+    return lib().oracle_max_threads()

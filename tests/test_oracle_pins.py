@@ -1,0 +1,497 @@
+"""Pins of the CPU oracle to facts fixed outside itself (no GPU needed).
+
+Each test checks the oracle against something the pages or the mathematics fix: the
+worked greedy round of the SDCP draft's Appendix A, the published Philox4x32-10
+known-answer vectors and a library implementation of Philox, the identities of Rules 1
+and 2 of SDCP Section 6.4 (full acceptance when q = p, 0 <= a <= M, greedy output
+independent of the proposal, Rule 2 at temperature 0 equal to Rule 1), the distribution
+preservation of Rule 2 (Monte Carlo chi-square against p), the expected tokens per round
+(the worked value 3.36 of "Inference: KV Cache, Batching, Speculative Decoding"), a
+rank-counting restatement of top-k/top-p on tiny rows, and the temperature power law.
+"""
+import json
+import math
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+from conftest import golden_path, ROOT
+
+PARAMS = None
+
+
+def _params(oracle_mod, B, rule=2, T=1000, k=0, p=1000, seed=0, round_=1, tags=None):
+    prm = np.zeros(B, dtype=oracle_mod.PARAMS_DTYPE)
+    prm["rule_id"] = rule
+    prm["temperature_milli"] = T
+    prm["top_k"] = k
+    prm["top_p_milli"] = p
+    prm["seed"] = seed
+    prm["round"] = round_
+    prm["session_tag"] = np.arange(B) if tags is None else tags
+    return prm
+
+
+def _offsets(Ms):
+    off = np.zeros(len(Ms) + 1, np.int32)
+    off[1:] = np.cumsum(Ms)
+    return off
+
+
+# ---------------------------------------------------------------------------------------
+# Philox4x32-10
+# ---------------------------------------------------------------------------------------
+def test_philox_known_answers(oracle_mod):
+    kat = json.load(open(golden_path("philox4x32_10_kat.json")))
+    for v in kat["vectors"]:
+        ctr = [int(h, 16) for h in v["counter"]]
+        key = [int(h, 16) for h in v["key"]]
+        out = oracle_mod.philox4x32_10(ctr, key)
+        assert [int(x) for x in out] == [int(h, 16) for h in v["out"]]
+
+
+_TRITON_SCRIPT = r"""
+import os, sys, json
+os.environ["TRITON_INTERPRET"] = "1"
+import torch, triton, triton.language as tl
+
+@triton.jit
+def _k(seedp, c0p, c1p, c2p, c3p, out):
+    c0 = tl.load(c0p); c1 = tl.load(c1p); c2 = tl.load(c2p); c3 = tl.load(c3p)
+    a, b, c, d = tl.philox(tl.load(seedp), c0, c1, c2, c3)
+    tl.store(out + 0, a); tl.store(out + 1, b); tl.store(out + 2, c); tl.store(out + 3, d)
+
+cases = json.loads(sys.stdin.read())
+res = []
+for ctr, key in cases:
+    seed = (key[1] << 32) | key[0]
+    if seed >= 2 ** 63:
+        seed -= 2 ** 64
+    sp = torch.tensor([seed], dtype=torch.int64)
+    cc = [torch.tensor([c], dtype=torch.int64).to(torch.int32) for c in ctr]
+    o = torch.zeros(4, dtype=torch.int32)
+    _k[(1,)](sp, *cc, o)
+    res.append([x & 0xFFFFFFFF for x in o.tolist()])
+print(json.dumps(res))
+"""
+
+
+def test_philox_matches_library_implementation(oracle_mod):
+    """Triton's tl.philox (run by its CPU interpreter) is an independent Philox4x32-10 with
+    the same key layout (low, high words of a 64-bit seed)."""
+    pytest.importorskip("triton")
+    rng = np.random.default_rng(7)
+    cases = [([int(v) for v in rng.integers(0, 2**32, 4)], [int(v) for v in rng.integers(0, 2**32, 2)])
+             for _ in range(24)]
+    cases.append(([3, 1, 17, 0x5D], [1000, 0]))
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    try:
+        out = subprocess.run([sys.executable, "-c", _TRITON_SCRIPT], input=json.dumps(cases),
+                             capture_output=True, text=True, timeout=600, env=env)
+    except subprocess.TimeoutExpired:
+        pytest.skip("triton interpreter too slow here")
+    if out.returncode != 0:
+        pytest.skip("triton interpreter unavailable: " + out.stderr.strip().splitlines()[-1][:200])
+    ref = json.loads(out.stdout.strip().splitlines()[-1])
+    for (ctr, key), r in zip(cases, ref):
+        assert [int(x) for x in oracle_mod.philox4x32_10(ctr, key)] == r
+
+
+def test_uniform_range_and_uniformity(oracle_mod):
+    """u in [0, 1), chi-square on 64 equal bins over 2^17 counters."""
+    n = 1 << 17
+    u = np.array([oracle_mod.uniform(12345, 3, i, i & 1, 0xABCDEF) for i in range(n)])
+    assert (u >= 0).all() and (u < 1).all()
+    h, _ = np.histogram(u, bins=64, range=(0, 1))
+    e = n / 64
+    chi2 = ((h - e) ** 2 / e).sum()
+    assert chi2 < 120  # 63 dof; p ~ 1e-5
+    # distinct purposes and positions give distinct values (counter-based, no reuse)
+    assert oracle_mod.uniform(1, 1, 0, 0, 0) != oracle_mod.uniform(1, 1, 0, 1, 0)
+    assert oracle_mod.uniform(1, 1, 0, 0, 0) != oracle_mod.uniform(1, 1, 1, 0, 0)
+    assert oracle_mod.uniform(1, 1, 0, 0, 0) != oracle_mod.uniform(1, 2, 0, 0, 0)
+
+
+# ---------------------------------------------------------------------------------------
+# Appendix A worked greedy round
+# ---------------------------------------------------------------------------------------
+def test_appendix_a_greedy_round(oracle_mod):
+    g = json.load(open(golden_path("appendix_a_greedy_round.json")))
+    rng = np.random.default_rng(1)
+    V = 16
+    M = len(g["proposal"])
+    argmaxes = g["target_argmax_per_position"]
+    target = rng.normal(0, 1, (M + 1, V)).astype(np.float32)
+    for i, t in enumerate(argmaxes):
+        target[i, t] = target[i].max() + 1.0
+    draft = rng.normal(0, 1, (M, V)).astype(np.float32)
+    res = oracle_mod.verify_batch(target, draft, _offsets([M]),
+                                  np.array(g["proposal"], np.int32),
+                                  _params(oracle_mod, 1, rule=1))
+    assert res["status"][0] == oracle_mod.S_OK
+    assert res["accepted"][0] == g["expected_accepted"]
+    n = res["n_out"][0]
+    assert list(res["out_tokens"][:n]) == g["expected_emitted"]
+    assert g["committed_before"] + n == g["expected_committed_after"]
+    assert list(res["out_tokens"][n:]) == [-1] * (M + 1 - n)
+
+
+# ---------------------------------------------------------------------------------------
+# Rule identities (SDCP Section 6.4)
+# ---------------------------------------------------------------------------------------
+def _random_batch(rng, B, V, Ms, sigma=2.0, noise=0.7, dtype=np.float32):
+    off = _offsets(Ms)
+    tot = int(off[-1])
+    target = rng.normal(0, sigma, (tot + B, V)).astype(np.float32)
+    draft = np.empty((tot, V), np.float32)
+    for b in range(B):
+        for i in range(Ms[b]):
+            draft[off[b] + i] = target[off[b] + b + i] + rng.normal(0, noise, V)
+    return target, draft, off
+
+
+def _sample_from(oracle_mod, rows, prm, rng):
+    toks = []
+    for r in rows:
+        d, _, _, _ = oracle_mod.row_dist(r, int(prm["temperature_milli"]), int(prm["top_k"]),
+                                         int(prm["top_p_milli"]))
+        toks.append(rng.choice(len(d), p=d / d.sum()))
+    return np.array(toks, np.int32)
+
+
+@pytest.mark.parametrize("T,k,p", [(1000, 0, 1000), (700, 5, 1000), (800, 0, 900), (1300, 7, 600)])
+def test_full_acceptance_when_q_equals_p(oracle_mod, T, k, p):
+    rng = np.random.default_rng(2)
+    B, V = 6, 40
+    Ms = [1, 3, 5, 2, 8, 4]
+    target, _, off = _random_batch(rng, B, V, Ms)
+    draft = np.empty((int(off[-1]), V), np.float32)
+    prm = _params(oracle_mod, B, rule=2, T=T, k=k, p=p, seed=99)
+    toks = np.zeros(int(off[-1]), np.int32)
+    for b in range(B):
+        for i in range(Ms[b]):
+            draft[off[b] + i] = target[off[b] + b + i]  # identical logits and profile
+        toks[off[b]:off[b + 1]] = _sample_from(oracle_mod, draft[off[b]:off[b + 1]], prm[b], rng)
+    res = oracle_mod.verify_batch(target, draft, off, toks, prm)
+    assert (res["status"] == 0).all()
+    assert (res["accepted"] == np.array(Ms)).all()
+    assert (res["n_out"] == np.array(Ms) + 1).all()
+    det = res["detail"]
+    for b in range(B):
+        assert det["extra_mode"][b] == oracle_mod.EXTRA_BONUS
+        # the bonus token is in the kept set of p[M+1]
+        _, kept, _, _ = oracle_mod.row_dist(target[off[b + 1] + b], T, k, p, want_kept=True)
+        assert kept[res["out_tokens"][off[b + 1] + b]] == 1
+
+
+def test_bounds_and_prefix(oracle_mod):
+    rng = np.random.default_rng(3)
+    B, V = 40, 30
+    Ms = list(rng.integers(1, 10, B))
+    target, draft, off = _random_batch(rng, B, V, Ms, noise=2.0)
+    prm = _params(oracle_mod, B, rule=2, T=900, seed=5)
+    prm["seed"] = np.arange(B) + 77
+    toks = np.concatenate([_sample_from(oracle_mod, draft[off[b]:off[b + 1]], prm[b], rng) for b in range(B)])
+    res = oracle_mod.verify_batch(target, draft, off, toks, prm)
+    a, n = res["accepted"], res["n_out"]
+    assert (res["status"] == 0).all()
+    assert ((0 <= a) & (a <= np.array(Ms))).all()
+    assert (n == a + 1).all()
+    for b in range(B):
+        s = off[b] + b
+        assert list(res["out_tokens"][s:s + a[b]]) == list(toks[off[b]:off[b] + a[b]])
+        assert 0 <= res["out_tokens"][s + a[b]] < V
+    assert (a < np.array(Ms)).any() and (a > 0).any()  # both outcomes occur
+
+
+def test_greedy_output_is_greedy_decoding(oracle_mod):
+    """Rule 1: the emitted tokens equal argmax decoding, whatever the drafter proposes."""
+    rng = np.random.default_rng(4)
+    B, V = 30, 12
+    Ms = list(rng.integers(1, 6, B))
+    target, draft, off = _random_batch(rng, B, V, Ms)
+    argm = target.argmax(axis=1)
+    toks = np.empty(int(off[-1]), np.int32)
+    for b in range(B):
+        for i in range(Ms[b]):
+            # propose the argmax with probability 1/2, else something else
+            t = argm[off[b] + b + i]
+            toks[off[b] + i] = t if rng.random() < 0.6 else (t + 1 + rng.integers(0, V - 1)) % V
+    res = oracle_mod.verify_batch(target, draft, off, toks, _params(oracle_mod, B, rule=1))
+    for b in range(B):
+        s = off[b] + b
+        n = res["n_out"][b]
+        assert list(res["out_tokens"][s:s + n]) == list(argm[s:s + n])
+        a = res["accepted"][b]
+        assert all(toks[off[b] + i] == argm[s + i] for i in range(a))
+        if a < Ms[b]:
+            assert toks[off[b] + a] != argm[s + a]
+
+
+def test_rule2_at_temperature_zero_equals_rule1(oracle_mod):
+    rng = np.random.default_rng(5)
+    B, V = 25, 20
+    Ms = list(rng.integers(1, 7, B))
+    target, draft, off = _random_batch(rng, B, V, Ms, noise=1.5)
+    toks = draft.argmax(axis=1).astype(np.int32)  # a T=0 drafter proposes its argmax
+    r1 = oracle_mod.verify_batch(target, draft, off, toks, _params(oracle_mod, B, rule=1))
+    r2 = oracle_mod.verify_batch(target, draft, off, toks, _params(oracle_mod, B, rule=2, T=0, seed=3))
+    for key in ("accepted", "n_out", "out_tokens", "status"):
+        assert (r1[key] == r2[key]).all(), key
+
+
+# ---------------------------------------------------------------------------------------
+# Distribution of Rule 2 (Monte Carlo over seeds, the oracle's own Philox stream)
+# ---------------------------------------------------------------------------------------
+def _chi2(counts, probs):
+    n = counts.sum()
+    e = probs * n
+    m = e > 0
+    return (((counts - e) ** 2)[m] / e[m]).sum(), int(m.sum()) - 1
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_rule2_output_distribution_is_p(oracle_mod, M):
+    """First emitted token ~ p[0]; after an accepted first token, the next ~ p[1]."""
+    rng = np.random.default_rng(10 + M)
+    V = 5
+    tl = [np.array([1.0, 0.2, -0.5, 0.7, -1.0], np.float32),
+          np.array([-0.3, 1.1, 0.4, -0.8, 0.0], np.float32),
+          np.array([0.5, -0.5, 1.5, 0.1, -2.0], np.float32)]
+    dl = [np.array([0.2, 1.0, -0.1, 0.9, 0.3], np.float32),
+          np.array([0.6, 0.2, 0.9, -0.4, -0.5], np.float32)]
+    Bn = 60000
+    prm = _params(oracle_mod, Bn, rule=2, T=1000)
+    prm["seed"] = np.arange(Bn, dtype=np.uint64) * 7919 + 11
+    target = np.concatenate([np.stack(tl[:M + 1])] * Bn)
+    draft = np.concatenate([np.stack(dl[:M])] * Bn)
+    off = _offsets([M] * Bn)
+    q = [oracle_mod.row_dist(d)[0] for d in dl[:M]]
+    p = [oracle_mod.row_dist(t)[0] for t in tl[:M + 1]]
+    toks = np.stack([rng.choice(V, size=Bn, p=q[i] / q[i].sum()) for i in range(M)], axis=1)
+    toks = toks.reshape(-1).astype(np.int32)
+    res = oracle_mod.verify_batch(target, draft, off, toks, prm, nthreads=8, want_detail=False)
+    assert (res["status"] == 0).all()
+    out = res["out_tokens"].reshape(Bn, M + 1)
+    first = np.bincount(out[:, 0], minlength=V)
+    c2, dof = _chi2(first, p[0])
+    assert c2 < 30, (c2, first, p[0] * Bn)  # 4 dof: p ~ 5e-6
+    sel = res["n_out"] >= 2
+    second = np.bincount(out[sel, 1], minlength=V)
+    c2b, _ = _chi2(second, p[1])
+    assert c2b < 30, (c2b, second, p[1] * sel.sum())
+
+
+def test_expected_tokens_per_round(oracle_mod):
+    """Mean n_out = (1 - alpha^(M+1)) / (1 - alpha) with alpha = sum_x min(p, q)."""
+    g = json.load(open(golden_path("expected_tokens_per_round.json")))
+    alpha, M = g["alpha"], g["k"]
+    # p = (0.9, 0.1), q = (0.7, 0.3): sum min = 0.8 at every position
+    lp = np.log(np.array([0.9, 0.1])).astype(np.float32)
+    lq = np.log(np.array([0.7, 0.3])).astype(np.float32)
+    pa = oracle_mod.row_dist(lp)[0]
+    qa = oracle_mod.row_dist(lq)[0]
+    assert abs(np.minimum(pa, qa).sum() - alpha) < 1e-6
+    closed = (1 - alpha ** (M + 1)) / (1 - alpha)
+    assert abs(closed - g["expected_tokens_per_round"]) < 0.005  # the page prints 2 decimals
+    Bn = 100000
+    rng = np.random.default_rng(21)
+    prm = _params(oracle_mod, Bn, rule=2)
+    prm["seed"] = np.arange(Bn, dtype=np.uint64) + 5
+    target = np.tile(lp, ((M + 1) * Bn, 1))
+    draft = np.tile(lq, (M * Bn, 1))
+    toks = rng.choice(2, size=M * Bn, p=qa).astype(np.int32)
+    res = oracle_mod.verify_batch(target, draft, _offsets([M] * Bn), toks, prm, nthreads=8,
+                                  want_detail=False)
+    mean = res["n_out"].mean()
+    se = res["n_out"].std() / math.sqrt(Bn)
+    assert abs(mean - closed) < 5 * se, (mean, se, closed)
+    assert abs(round(mean, 2) - g["expected_tokens_per_round"]) <= 0.01
+
+
+# ---------------------------------------------------------------------------------------
+# Sampling profile (SDCP Section 4.1)
+# ---------------------------------------------------------------------------------------
+def _rank_count_profile(l, T, k, p):
+    """Independent restatement without sorting: rank of j = number of ids before j in the
+    order (logit desc, id asc); top-k keeps rank < k; top-p keeps j when the mass of the
+    ids strictly before it (within top-k) is < P."""
+    V = len(l)
+    rank = np.array([sum(1 for i in range(V) if l[i] > l[j] or (l[i] == l[j] and i < j))
+                     for j in range(V)])
+    kk = V if (k == 0 or k >= V) else k
+    in_k = rank < kk
+    z = l.astype(np.float64) / (T / 1000.0)
+    w = np.where(in_k, np.exp(z - z.max()), 0.0)
+    pi = w / w.sum()
+    if p >= 1000:
+        kept = in_k
+        margin = np.inf
+    else:
+        P = p / 1000.0
+        before = np.array([pi[(rank < rank[j]) & in_k].sum() for j in range(V)])
+        kept = in_k & (before < P)
+        margin = np.min(np.abs(before[in_k] - P))
+    d = np.where(kept, pi, 0.0)
+    return d / d.sum(), kept, margin
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_profile_against_rank_counting(oracle_mod, seed):
+    rng = np.random.default_rng(100 + seed)
+    V = int(rng.integers(2, 14))
+    l = rng.integers(-3, 4, V).astype(np.float32) * 0.5  # many ties
+    T = int(rng.choice([300, 700, 1000, 1500]))
+    k = int(rng.choice([0, 1, 2, 3, 5, V + 3]))
+    p = int(rng.choice([1000, 999, 900, 500, 100, 1]))
+    ref, kept_ref, margin = _rank_count_profile(l, T, k, p)
+    if margin < 1e-9:
+        pytest.skip("crossing exactly on a boundary")
+    d, kept, info, rc = oracle_mod.row_dist(l, T, k, p, want_kept=True)
+    assert rc == 0
+    assert (kept.astype(bool) == kept_ref).all()
+    assert np.allclose(d, ref, rtol=1e-12, atol=1e-15)
+    assert info.kept == kept_ref.sum()
+    assert info.argmax == int(np.argmax(l))
+
+
+def test_temperature_power_law(oracle_mod):
+    """p at temperature T/2 is p at T squared and renormalised (no filters)."""
+    rng = np.random.default_rng(8)
+    l = rng.normal(0, 2, 50).astype(np.float32)
+    p1 = oracle_mod.row_dist(l, 1000)[0]
+    p2 = oracle_mod.row_dist(l, 500)[0]
+    sq = p1 ** 2 / (p1 ** 2).sum()
+    assert np.allclose(p2, sq, rtol=1e-12)
+
+
+def test_temperature_to_zero_is_argmax(oracle_mod):
+    l = np.array([0.0, 2.0, 1.9, 2.0, -1.0], np.float32)
+    d0 = oracle_mod.row_dist(l, 0)[0]
+    assert list(d0) == [0, 1, 0, 0, 0]  # ties to the smallest id
+    l2 = np.array([0.0, 2.0, 1.9, 1.98, -1.0], np.float32)
+    d = oracle_mod.row_dist(l2, 1)[0]  # T = 0.001
+    assert d[1] > 1 - 1e-6
+
+
+def test_top_p_crossing_token_is_kept(oracle_mod):
+    """Minimal prefix with cumulative >= P: equal logits give 0.25 steps, and P = 0.5 is
+    reached exactly by the second token, which is the last one kept."""
+    l = np.zeros(4, np.float32)
+    d, kept, info, _ = oracle_mod.row_dist(l, 1000, 0, 500, want_kept=True)
+    assert list(kept) == [1, 1, 0, 0] and info.kept == 2
+    assert list(d) == [0.5, 0.5, 0.0, 0.0]
+    d, kept, info, _ = oracle_mod.row_dist(l, 1000, 0, 501, want_kept=True)
+    assert info.kept == 3
+
+
+def test_draw_half_open_intervals(oracle_mod):
+    """u in [0,1) maps to token j iff C[j-1] <= u*W < C[j]: every token gets exactly its
+    weight, and a token of zero weight is never drawn (not even at u = 0)."""
+    w = np.array([0.0, 0.25, 0.25, 0.0, 0.5])
+    assert oracle_mod.draw(w, None, 0.0) == 1
+    assert oracle_mod.draw(w, None, 0.25) == 2
+    assert oracle_mod.draw(w, None, 0.5) == 4
+    assert oracle_mod.draw(w, None, 0.2499999) == 1
+    assert oracle_mod.draw(w, None, 0.9999999) == 4
+    # residual form: max(0, p - q)
+    p = np.array([0.5, 0.25, 0.25, 0.0])
+    q = np.array([0.5, 0.0, 0.5, 0.0])
+    assert oracle_mod.draw(p, q, 0.0) == 1 and oracle_mod.draw(p, q, 0.99) == 1
+
+
+def test_draw_cdf_total_variation(oracle_mod):
+    """sum max(0, p - q) equals half the L1 distance for normalised p, q."""
+    rng = np.random.default_rng(9)
+    p = rng.random(100); p /= p.sum()
+    q = rng.random(100); q /= q.sum()
+    C, W = oracle_mod.draw_cdf(p, q)
+    assert abs(W - 0.5 * np.abs(p - q).sum()) < 1e-12
+    assert (np.diff(C) >= 0).all()
+
+
+# ---------------------------------------------------------------------------------------
+# Statuses (SDCP Table 2) and degenerate inputs
+# ---------------------------------------------------------------------------------------
+def test_statuses(oracle_mod):
+    rng = np.random.default_rng(11)
+    V = 10
+    Ms = [2, 2, 2, 2, 2, 2, 2, 2]
+    B = len(Ms)
+    target, draft, off = _random_batch(rng, B, V, Ms)
+    toks = draft.argmax(axis=1).astype(np.int32)
+    prm = _params(oracle_mod, B, rule=2, T=1000)
+    prm["rule_id"][0] = 0                    # unknown rule
+    prm["rule_id"][1] = 3
+    prm["top_p_milli"][2] = 1001             # out of range
+    toks[off[3]] = V                          # token out of range
+    prm["top_k"][4] = 1                       # q(x) = 0 for a non-argmax token
+    toks[off[4] + 1] = (draft[off[4] + 1].argmax() + 1) % V
+    draft[off[5], toks[off[5]]] = -np.inf     # q(x) = 0 through a -inf logit
+    target[off[6] + 6 + 1, 3] = np.nan        # NaN in a scored row
+    res = oracle_mod.verify_batch(target, draft, off, toks, prm)
+    S = oracle_mod
+    assert list(res["status"]) == [S.S_BAD_PARAMS, S.S_BAD_PARAMS, S.S_BAD_PARAMS,
+                                   S.S_BAD_PROPOSAL, S.S_BAD_PROPOSAL, S.S_BAD_PROPOSAL,
+                                   S.S_BAD_PARAMS, S.S_OK]
+    for b in range(B - 1):
+        assert res["accepted"][b] == 0 and res["n_out"][b] == 0
+        assert (res["out_tokens"][off[b] + b: off[b + 1] + b + 1] == -1).all()
+    # limits on M, and Rule 2 without draft rows
+    Ms2 = [0, 65, 1]
+    off2 = _offsets(Ms2)
+    t2 = rng.normal(0, 1, (int(off2[-1]) + 3, V)).astype(np.float32)
+    d2 = rng.normal(0, 1, (int(off2[-1]), V)).astype(np.float32)
+    k2 = np.zeros(int(off2[-1]), np.int32)
+    r2 = oracle_mod.verify_batch(t2, d2, off2, k2, _params(oracle_mod, 3, rule=2))
+    assert list(r2["status"][:2]) == [S.S_LIMIT, S.S_LIMIT]
+    r3 = oracle_mod.verify_batch(t2, None, off2, k2, _params(oracle_mod, 3, rule=2))
+    assert r3["status"][2] == S.S_Q_UNAVAILABLE
+    r4 = oracle_mod.verify_batch(t2, None, off2, k2, _params(oracle_mod, 3, rule=1))
+    assert r4["status"][2] == S.S_OK
+
+
+def test_all_neg_inf_row_and_minus_inf_entries(oracle_mod):
+    V = 6
+    l = np.full(V, -np.inf, np.float32)
+    _, _, info, rc = oracle_mod.row_dist(l)
+    assert rc == 1 and info.invalid == 1
+    l2 = np.array([-np.inf, 1.0, -np.inf, 0.0, -np.inf, 1.0], np.float32)
+    d, _, info, rc = oracle_mod.row_dist(l2, 1000, 4, 1000)
+    assert rc == 0 and d[0] == 0 and d[2] == 0 and abs(d.sum() - 1) < 1e-15
+    assert info.argmax == 1
+
+
+def test_single_token_vocabulary(oracle_mod):
+    target = np.zeros((3, 1), np.float32)
+    draft = np.zeros((2, 1), np.float32)
+    res = oracle_mod.verify_batch(target, draft, _offsets([2]), np.zeros(2, np.int32),
+                                  _params(oracle_mod, 1, rule=2))
+    assert res["status"][0] == 0 and res["accepted"][0] == 2 and list(res["out_tokens"]) == [0, 0, 0]
+
+
+def test_bf16_input_widening(oracle_mod):
+    """A bf16 row (raw bits) gives the same result as its exact float32 widening."""
+    rng = np.random.default_rng(12)
+    f = rng.normal(0, 3, 64).astype(np.float32)
+    bits = (f.view(np.uint32) >> 16).astype(np.uint16)
+    widened = (bits.astype(np.uint32) << 16).view(np.float32)
+    d1, _, i1, _ = oracle_mod.row_dist(bits, 800, 10, 900)
+    d2, _, i2, _ = oracle_mod.row_dist(widened, 800, 10, 900)
+    assert (d1 == d2).all() and i1.kept == i2.kept and i1.argmax == i2.argmax
+
+
+def test_reproducible(oracle_mod):
+    rng = np.random.default_rng(13)
+    B, V = 10, 50
+    Ms = list(rng.integers(1, 9, B))
+    target, draft, off = _random_batch(rng, B, V, Ms)
+    prm = _params(oracle_mod, B, rule=2, T=800, k=20, p=950, seed=17)
+    toks = np.concatenate([_sample_from(oracle_mod, draft[off[b]:off[b + 1]], prm[b], rng) for b in range(B)])
+    r1 = oracle_mod.verify_batch(target, draft, off, toks, prm, nthreads=1)
+    r2 = oracle_mod.verify_batch(target, draft, off, toks, prm, nthreads=4)
+    for key in ("accepted", "n_out", "out_tokens", "status"):
+        assert (r1[key] == r2[key]).all()
