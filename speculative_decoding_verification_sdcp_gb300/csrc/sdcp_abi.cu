@@ -1,0 +1,127 @@
+// sdcp_abi.cu - the C ABI of libsdcp (declared in include/sdcp.h): argument checks on
+// the host, workspace layout, cluster sizes, and the two launches on the caller's stream.
+#include <climits>
+
+#include "sdcp_device.cuh"
+
+namespace sdcp {
+
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// CTAs per row cluster: about 32 KB of logits per CTA, 1..8.
+int row_cluster(int64_t V, int dtype) {
+  int64_t bytes = V * (dtype == SDCP_BF16 ? 2 : 4);
+  int64_t c = (bytes + 32767) / 32768;
+  return (int)(c < 1 ? 1 : (c > kMaxCluster ? kMaxCluster : c));
+}
+// CTAs per session cluster for the draw, and tiles per CTA (shared-memory prefix array).
+void session_cluster(int64_t V, int dtype, int* cluster, int* tiles_per_cta) {
+  const int64_t tile = (int64_t)kThreads * kEpt;
+  const int64_t nt = (V + tile - 1) / tile;
+  int64_t c = row_cluster(V, dtype);
+  int64_t need = (nt + 1023) / 1024;
+  if (c < need) c = need;
+  if (c > kMaxCluster) c = kMaxCluster;
+  *cluster = (int)c;
+  *tiles_per_cta = (int)((nt + c - 1) / c);
+}
+
+int check_common(const void* target, int dtype, int64_t V, int32_t B, const int32_t* m_offsets,
+                 int64_t total, const int32_t* tokens, const sdcp_session_params* params,
+                 const void* draft) {
+  if (B < 0 || total < 0 || V < 1) return SDCP_E_INVALID;
+  if (dtype != SDCP_F32 && dtype != SDCP_BF16) return SDCP_E_INVALID;
+  if (V > SDCP_MAX_VOCAB) return SDCP_E_TOO_LARGE;
+  if (total + B + total > (int64_t)INT32_MAX / kMaxCluster) return SDCP_E_TOO_LARGE;
+  if (B == 0) return SDCP_OK;
+  if (!target || !m_offsets || !params || (total > 0 && !tokens)) return SDCP_E_INVALID;
+  const size_t esz = dtype == SDCP_BF16 ? 2 : 4;
+  if (((uintptr_t)target % esz) != 0 || (draft && ((uintptr_t)draft % esz) != 0)) return SDCP_E_ALIGN;
+  return SDCP_OK;
+}
+
+size_t stats_bytes(int32_t B, int64_t total) {
+  return align256((size_t)(total + B + total) * sizeof(RowStat));
+}
+
+}  // namespace
+}  // namespace sdcp
+
+using namespace sdcp;
+
+extern "C" {
+
+int sdcp_abi_version(void) { return SDCP_ABI_VERSION; }
+
+const char* sdcp_strerror(int code) {
+  switch (code) {
+    case SDCP_OK: return "success";
+    case SDCP_E_INVALID: return "invalid argument (null pointer, negative size, V < 1 or unknown dtype)";
+    case SDCP_E_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case SDCP_E_ALIGN: return "logits pointer not aligned to its element size";
+    case SDCP_E_TOO_LARGE: return "vocabulary or row count above the supported maximum";
+    case SDCP_E_LAUNCH: return "CUDA kernel launch failed";
+    case SDCP_E_DEVICE: return "no usable CUDA device";
+    default: return "unknown sdcp error code";
+  }
+}
+
+size_t sdcp_workspace_bytes(int64_t V, int32_t B, int64_t total_drafts) {
+  if (B < 0 || total_drafts < 0 || V < 1 || V > SDCP_MAX_VOCAB) return 0;
+  return stats_bytes(B, total_drafts) + 256;
+}
+
+int sdcp_verify_batch(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
+                      int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                      const int32_t* draft_tokens, const sdcp_session_params* params,
+                      int32_t* accepted, int32_t* n_out, int32_t* out_tokens, int32_t* status,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens, params,
+                        draft_logits);
+  if (rc != SDCP_OK) return rc;
+  if (B == 0) return SDCP_OK;
+  if (!accepted || !n_out || !out_tokens || !status) return SDCP_E_INVALID;
+  if (!workspace || ((uintptr_t)workspace & 255u) != 0 ||
+      workspace_bytes < sdcp_workspace_bytes(V, B, total_drafts))
+    return SDCP_E_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  RowStat* stats = reinterpret_cast<RowStat*>(workspace);
+
+  RowArgs ra{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
+             stats, nullptr, 0};
+  if (launch_row_stats(ra, dtype, row_cluster(V, dtype), s) != 0) return SDCP_E_LAUNCH;
+  int c2, tiles;
+  session_cluster(V, dtype, &c2, &tiles);
+  SessArgs sa{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
+              stats, accepted, n_out, out_tokens, status, tiles};
+  if (launch_sessions(sa, dtype, c2, s) != 0) return SDCP_E_LAUNCH;
+  if (cudaGetLastError() != cudaSuccess) return SDCP_E_LAUNCH;
+  return SDCP_OK;
+}
+
+int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
+                   int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                   const int32_t* draft_tokens, const sdcp_session_params* params,
+                   sdcp_row_stat* stats_out, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  int rc = check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens, params,
+                        draft_logits);
+  if (rc != SDCP_OK) return rc;
+  if (B == 0) return SDCP_OK;
+  if (!stats_out) return SDCP_E_INVALID;
+  if (total_drafts > 0 && !draft_logits) return SDCP_E_INVALID;
+  if (!workspace || ((uintptr_t)workspace & 255u) != 0 ||
+      workspace_bytes < sdcp_workspace_bytes(V, B, total_drafts))
+    return SDCP_E_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  RowArgs ra{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
+             reinterpret_cast<RowStat*>(workspace), stats_out, 1};
+  if (launch_row_stats(ra, dtype, row_cluster(V, dtype), s) != 0) return SDCP_E_LAUNCH;
+  if (cudaGetLastError() != cudaSuccess) return SDCP_E_LAUNCH;
+  return SDCP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,374 @@
+// sdcp_device.cuh - device helpers of libsdcp (sm_103a): order keys, Philox4x32-10,
+// deterministic block reductions and scans, row slicing.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sdcp.h"
+
+namespace sdcp {
+
+namespace cg = cooperative_groups;
+
+constexpr int kThreads = 256;          // threads per CTA of both kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kWindowBins = 2048;      // exact bf16 keys below the row maximum
+constexpr int kTieListCap = 256;       // ids with the cut key, per CTA
+constexpr int kMaxCluster = 8;
+constexpr int kEpt = 8;                // elements per thread per tile (draw kernel)
+
+// Internal per-row record written by the row kernel (workspace), 32 bytes.
+struct RowStat {
+  float lmax;        // largest logit of the row
+  float s;           // sum over the kept set of exp((l - lmax) * 1000/T); 1 at T = 0
+  float dlx;         // l[x] - lmax for the row's draft token (-inf: x has a -inf logit)
+  int32_t argmax;    // smallest id of the largest logit (rows that need it)
+  uint32_t thr_key;  // kept iff key > thr_key, or key == thr_key and id <= thr_id
+  int32_t thr_id;
+  int32_t kept;      // size of the kept set
+  uint32_t flags;    // SDCP_ROW_* plus kRowHasX
+};
+constexpr uint32_t kRowHasX = 16u;     // the row carries a draft token that is in range
+
+static_assert(sizeof(RowStat) == 32, "RowStat layout");
+
+// Arguments of the row kernel (phase 1).
+struct RowArgs {
+  const void* target;
+  const void* draft;
+  int64_t V;
+  int32_t B;
+  const int32_t* m_offsets;
+  int64_t total;              // sum of M (host value)
+  const int32_t* tokens;
+  const sdcp_session_params* params;
+  RowStat* stats;             // [total + B + total]: target rows, then draft rows
+  sdcp_row_stat* pub;         // optional public copy (statistics mode)
+  int stats_mode;             // 1: every row gets the full statistics
+};
+
+// Arguments of the session kernel (phase 2).
+struct SessArgs {
+  const void* target;
+  const void* draft;
+  int64_t V;
+  int32_t B;
+  const int32_t* m_offsets;
+  int64_t total;
+  const int32_t* tokens;
+  const sdcp_session_params* params;
+  const RowStat* stats;
+  int32_t* accepted;
+  int32_t* n_out;
+  int32_t* out_tokens;
+  int32_t* status;
+  int max_tiles_per_cta;      // length of the per-CTA tile prefix array (dynamic smem)
+};
+
+int launch_row_stats(const RowArgs& a, int dtype, int cluster, cudaStream_t stream);
+int launch_sessions(const SessArgs& a, int dtype, int cluster, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------------
+// Order key of a binary32 bit pattern: unsigned order of keys = numeric order of the
+// values, -0 and +0 share a key (so ties between them go to the smaller id).
+// Positive x: bits | 2^31.  Negative x: -bits (two's complement), which maps -0 onto
+// +0's key and keeps every other negative value below it.
+// +inf -> 0xFF800000, -inf -> 0x00800000; NaNs fall outside [0x00800000, 0xFF800000].
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key(uint32_t bits) {
+  uint32_t t = (uint32_t)((int32_t)bits >> 31);
+  return (bits ^ (t | 0x80000000u)) - t;
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  uint32_t bits = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : (0u - key);
+  return __uint_as_float(bits);
+}
+constexpr uint32_t kKeyPosInf = 0xFF800000u;
+constexpr uint32_t kKeyNegInf = 0x00800000u;
+
+// 2^x on the SFU (PTX ex2.approx, flush-to-zero; ~2 ulp relative).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// max that propagates NaN (PTX max.NaN).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float y;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
+
+// ---------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): per round the pair of 32x32->64
+// products with multipliers 0xD2511F53 (of word 0) and 0xCD9E8D57 (of word 2) is mixed
+// with words 1 and 3 and the key; the key advances by 0x9E3779B9 / 0xBB67AE85.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
+    uint32_t h0 = __umulhi(m0, c.x), l0 = m0 * c.x;
+    uint32_t h1 = __umulhi(m1, c.z), l1 = m1 * c.z;
+    c = make_uint4(h1 ^ c.y ^ k.x, l1, h0 ^ c.w ^ k.y, l0);
+    k.x += 0x9E3779B9u;
+    k.y += 0xBB67AE85u;
+  }
+  return c;
+}
+// The verifier's uniform for (position, purpose) of one session: 53 bits / 2^53.
+__device__ __forceinline__ double verifier_uniform(const sdcp_session_params& p,
+                                                   uint32_t position, uint32_t purpose) {
+  uint4 w = philox4x32_10(make_uint4(position, purpose, p.round, p.session_tag),
+                          make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
+  unsigned long long bits = ((unsigned long long)w.x << 21) | (unsigned long long)(w.y >> 11);
+  return (double)bits * 0x1.0p-53;
+}
+
+// ---------------------------------------------------------------------------------
+// Element access.
+// ---------------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kPerVec = 4;
+  __device__ __forceinline__ static uint32_t bits(float v) { return __float_as_uint(v); }
+  __device__ __forceinline__ static void unpack(const uint4& q, uint32_t (&b)[4]) {
+    b[0] = q.x; b[1] = q.y; b[2] = q.z; b[3] = q.w;
+  }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int kPerVec = 8;
+  __device__ __forceinline__ static uint32_t bits(__nv_bfloat16 v) {
+    return ((uint32_t)__bfloat16_as_ushort(v)) << 16;
+  }
+  __device__ __forceinline__ static void unpack(const uint4& q, uint32_t (&b)[8]) {
+    b[0] = q.x << 16; b[1] = q.x & 0xFFFF0000u;
+    b[2] = q.y << 16; b[3] = q.y & 0xFFFF0000u;
+    b[4] = q.z << 16; b[5] = q.z & 0xFFFF0000u;
+    b[6] = q.w << 16; b[7] = q.w & 0xFFFF0000u;
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ uint32_t load_bits(const T* row, int64_t j) {
+  return Elem<T>::bits(row[j]);
+}
+
+// Streaming 16-byte load that does not allocate in L1.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// A row split into: head (scalar elements up to the first 16-byte boundary), nvec full
+// 16-byte vectors, and a scalar tail.
+struct RowLayout {
+  int64_t head, nvec, tail0;  // tail elements are [tail0, V)
+};
+template <typename T>
+__device__ __forceinline__ RowLayout row_layout(const T* row, int64_t V) {
+  constexpr int E = Elem<T>::kPerVec;
+  uintptr_t a = (uintptr_t)row;
+  int64_t head = (int64_t)(((16u - (uint32_t)(a & 15u)) & 15u) / sizeof(T));
+  if (head > V) head = V;
+  int64_t nvec = (V - head) / E;
+  RowLayout L;
+  L.head = head;
+  L.nvec = nvec;
+  L.tail0 = head + nvec * E;
+  return L;
+}
+
+// ---------------------------------------------------------------------------------
+// Deterministic reductions: fixed butterfly per warp, then warp 0 over the warp results.
+// ---------------------------------------------------------------------------------
+template <typename F>
+__device__ __forceinline__ float warp_reduce(float v, F op) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+__device__ __forceinline__ int64_t warp_max_i64(int64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, (int64_t)__shfl_xor_sync(0xFFFFFFFFu, (long long)v, o));
+  return v;
+}
+__device__ __forceinline__ int64_t warp_min_i64(int64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, (int64_t)__shfl_xor_sync(0xFFFFFFFFu, (long long)v, o));
+  return v;
+}
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Block-wide (kThreads) reductions through a small shared scratch; all threads get the
+// result.  Scratch must hold kWarps elements and is reused after a barrier.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+  v = warp_reduce(v, [](float a, float b) { return a + b; });
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  float r = 0.f;
+  if (w == 0) {
+    r = (l < kWarps) ? scratch[l] : 0.f;
+    r = warp_reduce(r, [](float a, float b) { return a + b; });
+    if (l == 0) scratch[0] = r;
+  }
+  __syncthreads();
+  r = scratch[0];
+  return r;
+}
+__device__ __forceinline__ long long block_sum_ll(long long v, long long* scratch) {
+  v = warp_sum_ll(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  long long r = 0;
+  if (w == 0) {
+    r = (l < kWarps) ? scratch[l] : 0;
+    r = warp_sum_ll(r);
+    if (l == 0) scratch[0] = r;
+  }
+  __syncthreads();
+  r = scratch[0];
+  return r;
+}
+__device__ __forceinline__ int64_t block_max_i64(int64_t v, long long* scratch) {
+  v = warp_max_i64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int64_t r = (l < kWarps) ? (int64_t)scratch[l] : INT64_MIN;
+    r = warp_max_i64(r);
+    if (l == 0) scratch[0] = r;
+  }
+  __syncthreads();
+  return (int64_t)scratch[0];
+}
+__device__ __forceinline__ int64_t block_min_i64(int64_t v, long long* scratch) {
+  v = warp_min_i64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int64_t r = (l < kWarps) ? (int64_t)scratch[l] : INT64_MAX;
+    r = warp_min_i64(r);
+    if (l == 0) scratch[0] = r;
+  }
+  __syncthreads();
+  return (int64_t)scratch[0];
+}
+
+// Exclusive scan of one float per thread (block of kThreads), fixed association.
+// Returns the exclusive prefix; *total gets the sum over the block.
+__device__ __forceinline__ float block_exclusive_scan(float v, float* scratch, float* total) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  float incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    float t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (l >= o) incl += t;
+  }
+  __syncthreads();
+  if (l == 31) scratch[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    float s = (l < kWarps) ? scratch[l] : 0.f;
+    float si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      float t = __shfl_up_sync(0xFFFFFFFFu, si, o);
+      if (l >= o) si += t;
+    }
+    float se = __shfl_up_sync(0xFFFFFFFFu, si, 1);
+    if (l < kWarps) scratch[kWarps + l] = (l == 0) ? 0.f : se;  // exclusive warp offsets
+    if (l == kWarps - 1) scratch[2 * kWarps] = si;
+  }
+  __syncthreads();
+  float excl_in_warp = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (l == 0) excl_in_warp = 0.f;
+  float r = (w == 0) ? excl_in_warp : scratch[kWarps + w] + excl_in_warp;
+  *total = scratch[2 * kWarps];
+  return r;
+}
+// Same for 64-bit integers (exact).
+__device__ __forceinline__ long long block_exclusive_scan_ll(long long v, long long* scratch,
+                                                             long long* total) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (l >= o) incl += t;
+  }
+  __syncthreads();
+  if (l == 31) scratch[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    long long s = (l < kWarps) ? scratch[l] : 0;
+    long long si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      long long t = __shfl_up_sync(0xFFFFFFFFu, si, o);
+      if (l >= o) si += t;
+    }
+    long long se = __shfl_up_sync(0xFFFFFFFFu, si, 1);
+    if (l < kWarps) scratch[kWarps + l] = (l == 0) ? 0 : se;
+    if (l == kWarps - 1) scratch[2 * kWarps] = si;
+  }
+  __syncthreads();
+  long long ew = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (l == 0) ew = 0;
+  long long r = scratch[kWarps + w] + ew;
+  *total = scratch[2 * kWarps];
+  return r;
+}
+
+// Session of a row by a warp-cooperative 32-ary search over m_offsets: the largest b in
+// [0, B) with key(b) <= r, key(b) = m_offsets[b] + (target ? b : 0).  Clamped to [0, B).
+__device__ __forceinline__ int32_t find_session(const int32_t* __restrict__ m_offsets, int32_t B,
+                                                int64_t r, bool target) {
+  int64_t lo = 0, hi = B;
+  const int l = threadIdx.x & 31;
+  while (hi - lo > 1) {
+    int64_t step = (hi - lo + 31) / 32;
+    int64_t j = lo + (int64_t)l * step;
+    bool ok = false;
+    if (j < hi) {
+      int64_t k = (int64_t)__ldg(&m_offsets[j]) + (target ? j : 0);
+      ok = (k <= r);
+    }
+    unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
+    int last = (m == 0) ? 0 : (31 - __clz(m));
+    int64_t nlo = lo + (int64_t)last * step;
+    int64_t nhi = nlo + step;
+    lo = nlo;
+    hi = nhi < hi ? nhi : hi;
+  }
+  return (int32_t)lo;
+}
+
+}  // namespace sdcp

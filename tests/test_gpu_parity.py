@@ -1,0 +1,234 @@
+"""GPU path (libsdcp through its C ABI) against the CPU oracle, element by element.
+
+Small batches are compared whole (every session, every row statistic); the five
+workload sizes of the benchmark are run whole on the GPU in the benchmark's launch
+configuration, checked for the properties of SDCP Sections 5.2 and 6.4 on every session,
+and compared with the oracle on a sample of sessions.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+from speculative_decoding_verification_sdcp_gb300 import synth  # noqa: E402
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_verification_sdcp_gb300 import build_ext
+    build_ext.build()
+    import oracle
+    oracle.build()
+
+
+def _parity(batch, rows=True, with_draft=True):
+    import oracle
+    import parity
+    got = parity.run_gpu(batch, with_draft=with_draft)
+    T, D, off, x = parity.host_arrays(batch)
+    ref = oracle.verify_batch(T, D if with_draft else None, off, x, batch.params, nthreads=8)
+    counts = parity.compare_verdicts(got, ref, T, D, off, x, batch.params)
+    parity.check_invariants(got, off, x, batch.params, batch.V)
+    if rows:
+        gs = parity.gpu_row_stats(batch)
+        counts["rows"] = parity.compare_row_stats(gs, T, D, off, x, batch.params, batch.dtype_code)
+    return got, counts
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_greedy"])
+def test_tiny_workloads(name):
+    batch = synth.make_batch(synth.WORKLOADS[name], device=DEV)
+    _, counts = _parity(batch)
+    assert counts["exact"] == batch.B, counts
+
+
+CASES = [
+    # dtype, V, M, rules, T, top_k, top_p, sigma, noise
+    (synth.F32, 1, 3, "spec", 1000, 0, 1000, 1.0, 0.5),
+    (synth.F32, 7, 5, "alternate", 1000, 0, 1000, 1.0, 0.5),
+    (synth.BF16, 7, 5, "alternate", 700, 3, 1000, 1.0, 0.5),
+    (synth.F32, 64, ("uniform", 1, 12), "spec", 600, 0, 900, 2.0, 1.0),
+    (synth.BF16, 1000, ("uniform", 1, 64), "alternate", 1000, 0, 1000, 2.0, 0.5),
+    (synth.BF16, 4099, 6, "spec", 800, 50, 1000, 3.0, 1.0),       # ragged rows (unaligned)
+    (synth.BF16, 4099, 6, "spec", 800, 0, 900, 3.0, 1.0),
+    (synth.BF16, 4099, 6, "spec", 1300, 40, 700, 3.0, 1.0),
+    (synth.F32, 4099, 6, "spec", 800, 50, 900, 3.0, 1.0),          # fp32 filters: generic search
+    (synth.BF16, 32000, 8, "spec", 700, 50, 1000, 3.0, 1.0),
+    (synth.BF16, 32000, 4, "spec", 0, 0, 1000, 3.0, 1.0),          # temperature 0 under Rule 2
+    (synth.BF16, 50257, ("uniform", 1, 9), "spec", 1000, 1, 1000, 3.0, 1.0),
+    (synth.F32, 50257, 3, "alternate", 1700, 0, 1000, 3.0, 1.0),
+    (synth.BF16, 65536, 3, "spec", 900, 0, 1, 3.0, 1.0),           # top-p keeps only the argmax
+    (synth.BF16, 65536, 3, "spec", 900, 0, 999, 3.0, 1.0),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "dt%d-V%d-T%d-k%d-p%d-%s" % (c[0], c[1], c[4], c[5], c[6], c[3]))
+def test_small_matrix(case):
+    dt, V, m, rules, T, k, p, sigma, noise = case
+    w = synth.custom_workload(B=12, V=V, dtype=dt, m=m, rules=rules, temperature_milli=T, top_k=k,
+                              top_p_milli=p, sigma=sigma, noise=noise, seed_base=77,
+                              gen_seed=100 + CASES.index(case))
+    batch = synth.make_batch(w, device=DEV)
+    _, counts = _parity(batch)
+    assert counts["exact"] >= batch.B - 2, counts
+
+
+def test_ties_and_tie_overflow():
+    """Integer logits (many equal values) and a cut value shared by ~30000 tokens."""
+    B, V, M = 6, 32000, 3
+    w = synth.custom_workload(B=B, V=V, dtype=synth.BF16, m=M, rules="spec", temperature_milli=1000,
+                              top_k=100, top_p_milli=950, gen_seed=5)
+    batch = synth.make_batch(w, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(3)
+    t = torch.randint(-3, 4, batch.target.shape, generator=g, device=DEV).float()
+    t[:3] = 0.0
+    t[:3, :5] = 2.0
+    batch.target.copy_(t.to(torch.bfloat16))
+    batch.draft.copy_(batch.target[: batch.total_drafts].clone())
+    _parity(batch)
+
+
+def test_flat_distribution_window_fallback():
+    """Logits within +-0.05 straddle zero: the nucleus spans many binades below the max
+    and the window cannot hold it, so the generic search decides."""
+    w = synth.custom_workload(B=4, V=8192, dtype=synth.BF16, m=3, rules="spec", temperature_milli=1000,
+                              top_p_milli=900, sigma=0.02, noise=0.01, gen_seed=9)
+    batch = synth.make_batch(w, device=DEV)
+    _, counts = _parity(batch)
+    assert counts["rows"]["fallback"] > 0
+
+
+def test_statuses_and_degenerate_rows():
+    import oracle
+    import parity
+    B, V, M = 9, 40, 2
+    w = synth.custom_workload(B=B, V=V, dtype=synth.F32, m=M, rules="spec", gen_seed=11)
+    batch = synth.make_batch(w, device=DEV)
+    off = batch.m_offsets.cpu().numpy()
+    prm = batch.params.copy()
+    prm["rule_id"][0] = 0
+    prm["rule_id"][1] = 3
+    prm["top_p_milli"][2] = 1001
+    x = batch.draft_tokens.cpu().numpy().copy()
+    x[off[3]] = V                                   # token out of range
+    prm["top_k"][4] = 1                             # q(x) = 0 unless x is the draft argmax
+    dargs = batch.draft.cpu().numpy()
+    x[off[4] + 1] = (int(np.argmax(dargs[off[4] + 1])) + 1) % V
+    batch.draft[off[5], int(x[off[5]])] = -float("inf")   # q(x) = 0 through -inf
+    batch.target[off[6] + 6 + 1, 3] = float("nan")         # NaN in a scored row
+    batch.target[off[7] + 7 + 2, :] = -float("inf")        # a row without a finite logit
+    batch.draft_tokens.copy_(torch.from_numpy(x))
+    batch.params = prm
+    batch.params_dev = synth.params_to_device(prm, DEV)
+    got, _ = _parity(batch, rows=False)
+    S = oracle
+    assert list(got["status"]) == [S.S_BAD_PARAMS, S.S_BAD_PARAMS, S.S_BAD_PARAMS, S.S_BAD_PROPOSAL,
+                                   S.S_BAD_PROPOSAL, S.S_BAD_PROPOSAL, S.S_BAD_PARAMS,
+                                   S.S_BAD_PARAMS, S.S_OK]
+    # Rule 2 without draft logits, and greedy sessions without them
+    got2 = parity.run_gpu(batch, with_draft=False)
+    ref2 = oracle.verify_batch(*parity.host_arrays(batch)[:1], None, off, x, prm)
+    assert np.array_equal(got2["status"], ref2["status"])
+
+
+def test_limits_on_m():
+    import oracle
+    import parity
+    V = 16
+    Ms = [0, 65, 64, 1]
+    off = np.zeros(len(Ms) + 1, np.int32)
+    off[1:] = np.cumsum(Ms)
+    tot = int(off[-1])
+    g = torch.Generator(device=DEV).manual_seed(1)
+    T = torch.randn(tot + len(Ms), V, generator=g, device=DEV)
+    D = torch.randn(tot, V, generator=g, device=DEV)
+    x = torch.randint(0, V, (tot,), generator=g, device=DEV, dtype=torch.int32)
+    prm = np.zeros(len(Ms), dtype=synth.PARAMS_DTYPE)
+    prm["rule_id"] = 1
+    prm["temperature_milli"] = 1000
+    prm["top_p_milli"] = 1000
+    w = synth.custom_workload(B=len(Ms), V=V)
+    batch = synth.Batch(w, T, D, torch.from_numpy(off).to(DEV), x, prm, synth.params_to_device(prm, DEV))
+    got = parity.run_gpu(batch)
+    ref = oracle.verify_batch(T.cpu().numpy(), D.cpu().numpy(), off, x.cpu().numpy(), prm)
+    for k in ("status", "accepted", "n_out", "out_tokens"):
+        assert np.array_equal(got[k], ref[k]), k
+    assert list(got["status"][:2]) == [oracle.S_LIMIT, oracle.S_LIMIT]
+
+
+def test_empty_batch():
+    from speculative_decoding_verification_sdcp_gb300 import sdcp
+    z = torch.empty(0, dtype=torch.int32, device=DEV)
+    t = torch.empty(0, 8, dtype=torch.float32, device=DEV)
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    sdcp.sdcp_verify_batch(t, t, torch.zeros(1, dtype=torch.int32, device=DEV), 0, z,
+                           torch.empty(0, dtype=torch.uint8, device=DEV), z, z, z, z, ws)
+
+
+def test_reproducible_bit_for_bit():
+    import parity
+    batch = synth.make_batch(synth.custom_workload(B=16, V=32000, dtype=synth.BF16, m=("uniform", 1, 16),
+                                                   rules="spec", temperature_milli=800, top_p_milli=900,
+                                                   sigma=3.0, noise=0.8, gen_seed=4), device=DEV)
+    a = parity.run_gpu(batch)
+    b = parity.run_gpu(batch)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_large_vocabulary():
+    batch = synth.make_batch(synth.custom_workload(B=3, V=1 << 20, dtype=synth.BF16, m=2, rules="spec",
+                                                   temperature_milli=1000, top_k=1000, sigma=3.0,
+                                                   noise=1.0, gen_seed=6), device=DEV)
+    _parity(batch)
+
+
+SAMPLE = {"topk50": 16, "topp90_ragged": 12, "large_batch_mixed": 24, "mmax_stress": 3}
+
+
+@pytest.mark.parametrize("name", ["topk50", "topp90_ragged", "large_batch_mixed", "mmax_stress"])
+def test_full_size_workloads(name):
+    """Whole batch on the GPU (the benchmark's call); the oracle re-runs sampled sessions."""
+    import oracle
+    import parity
+    w = synth.WORKLOADS[name]
+    batch = synth.make_batch(w, device=DEV)
+    got = parity.run_gpu(batch)
+    T_dev, off, x = batch.target, batch.m_offsets.cpu().numpy(), batch.draft_tokens.cpu().numpy()
+    assert (got["status"] == 0).all(), np.unique(got["status"], return_counts=True)
+    parity.check_invariants(got, off, x, batch.params, batch.V)
+    rng = np.random.default_rng(0)
+    k = SAMPLE[name]
+    sessions = sorted(set([0, batch.B - 1] + list(rng.choice(batch.B, size=k - 2, replace=False))))
+    Ts, Ds, offs, xs, prms = parity.sub_batch(batch, sessions)
+    ref = oracle.verify_batch(Ts, Ds, offs, xs, prms, nthreads=8)
+    sub = {"status": got["status"][sessions], "accepted": got["accepted"][sessions],
+           "n_out": got["n_out"][sessions]}
+    toks = []
+    for b in sessions:
+        o0, o1 = int(off[b]), int(off[b + 1])
+        toks.append(got["out_tokens"][o0 + b:o1 + b + 1])
+    sub["out_tokens"] = np.concatenate(toks)
+    counts = parity.compare_verdicts(sub, ref, Ts, Ds, offs, xs, prms)
+    # row statistics of the sampled sessions' rows
+    gs = parity.gpu_row_stats(batch)
+    B, tot = batch.B, batch.total_drafts
+    rows_full, rows_sub = [], []
+    sub_off = offs
+    for si, b in enumerate(sessions):
+        o0, o1 = int(off[b]), int(off[b + 1])
+        s0 = int(sub_off[si])
+        for i in range(o1 - o0 + 1):
+            rows_full.append(o0 + b + i); rows_sub.append(s0 + si + i)
+        for i in range(o1 - o0):
+            rows_full.append(tot + B + o0 + i); rows_sub.append(int(sub_off[-1]) + len(sessions) + s0 + i)
+    gsub = np.zeros(len(Ts) + len(Ds), dtype=gs.dtype)
+    gsub[rows_sub] = gs[rows_full]
+    rc = parity.compare_row_stats(gsub, Ts, Ds, offs, xs, prms, batch.dtype_code, rows=rows_sub)
+    assert rc["fallback"] == 0, rc
+    print(name, counts, rc)
