@@ -145,6 +145,26 @@ int sdcp_verify_batch(const void* target_logits, const void* draft_logits, int d
                       void* stream);
 
 /*
+ * The two phases of sdcp_verify_batch as separate calls (same arguments, same workspace):
+ * phase 1 (sdcp_verify_rows) computes the statistics of every scored row of the sampling
+ * profile (Section 4.1) into the workspace; phase 2 (sdcp_verify_sessions) runs the
+ * precondition, the acceptance tests, the first-rejection scan and the draw of the
+ * additional token (Sections 6.3, 6.4) and writes the outputs.  Calling phase 1 then
+ * phase 2 on one stream is exactly sdcp_verify_batch; a profiler or a scheduler can put an
+ * event between them.  Return codes as for sdcp_verify_batch.
+ */
+int sdcp_verify_rows(const void* target_logits, const void* draft_logits, int dtype,
+                     int64_t V, int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                     const int32_t* draft_tokens, const sdcp_session_params* params,
+                     void* workspace, size_t workspace_bytes, void* stream);
+int sdcp_verify_sessions(const void* target_logits, const void* draft_logits, int dtype,
+                         int64_t V, int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                         const int32_t* draft_tokens, const sdcp_session_params* params,
+                         int32_t* accepted, int32_t* n_out, int32_t* out_tokens,
+                         int32_t* status, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
  * Per-row statistics of the sampling profile (parity hook for the first phase).
  *
  * Same inputs as sdcp_verify_batch.  For every target row r (0 <= r < total_drafts + B)

@@ -74,11 +74,29 @@ size_t sdcp_workspace_bytes(int64_t V, int32_t B, int64_t total_drafts) {
   return stats_bytes(B, total_drafts) + 256;
 }
 
-int sdcp_verify_batch(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
-                      int32_t B, const int32_t* m_offsets, int64_t total_drafts,
-                      const int32_t* draft_tokens, const sdcp_session_params* params,
-                      int32_t* accepted, int32_t* n_out, int32_t* out_tokens, int32_t* status,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+int sdcp_verify_rows(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
+                     int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                     const int32_t* draft_tokens, const sdcp_session_params* params,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens, params,
+                        draft_logits);
+  if (rc != SDCP_OK) return rc;
+  if (B == 0) return SDCP_OK;
+  if (!workspace || ((uintptr_t)workspace & 255u) != 0 ||
+      workspace_bytes < sdcp_workspace_bytes(V, B, total_drafts))
+    return SDCP_E_WORKSPACE;
+  RowArgs ra{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
+             reinterpret_cast<RowStat*>(workspace), nullptr, 0};
+  if (launch_row_stats(ra, dtype, row_cluster(V, dtype), reinterpret_cast<cudaStream_t>(stream)) != 0)
+    return SDCP_E_LAUNCH;
+  return SDCP_OK;
+}
+
+int sdcp_verify_sessions(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
+                         int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                         const int32_t* draft_tokens, const sdcp_session_params* params,
+                         int32_t* accepted, int32_t* n_out, int32_t* out_tokens, int32_t* status,
+                         void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens, params,
                         draft_logits);
   if (rc != SDCP_OK) return rc;
@@ -87,19 +105,30 @@ int sdcp_verify_batch(const void* target_logits, const void* draft_logits, int d
   if (!workspace || ((uintptr_t)workspace & 255u) != 0 ||
       workspace_bytes < sdcp_workspace_bytes(V, B, total_drafts))
     return SDCP_E_WORKSPACE;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  RowStat* stats = reinterpret_cast<RowStat*>(workspace);
-
-  RowArgs ra{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
-             stats, nullptr, 0};
-  if (launch_row_stats(ra, dtype, row_cluster(V, dtype), s) != 0) return SDCP_E_LAUNCH;
   int c2, tiles;
   session_cluster(V, dtype, &c2, &tiles);
   SessArgs sa{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
-              stats, accepted, n_out, out_tokens, status, tiles};
-  if (launch_sessions(sa, dtype, c2, s) != 0) return SDCP_E_LAUNCH;
-  if (cudaGetLastError() != cudaSuccess) return SDCP_E_LAUNCH;
+              reinterpret_cast<const RowStat*>(workspace), accepted, n_out, out_tokens, status, tiles};
+  if (launch_sessions(sa, dtype, c2, reinterpret_cast<cudaStream_t>(stream)) != 0) return SDCP_E_LAUNCH;
   return SDCP_OK;
+}
+
+int sdcp_verify_batch(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
+                      int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                      const int32_t* draft_tokens, const sdcp_session_params* params,
+                      int32_t* accepted, int32_t* n_out, int32_t* out_tokens, int32_t* status,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (B > 0 && (!accepted || !n_out || !out_tokens || !status)) {
+    int rc = check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens,
+                          params, draft_logits);
+    return rc != SDCP_OK ? rc : SDCP_E_INVALID;
+  }
+  int rc = sdcp_verify_rows(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
+                            draft_tokens, params, workspace, workspace_bytes, stream);
+  if (rc != SDCP_OK || B == 0) return rc;
+  return sdcp_verify_sessions(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
+                              draft_tokens, params, accepted, n_out, out_tokens, status, workspace,
+                              workspace_bytes, stream);
 }
 
 int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtype, int64_t V,

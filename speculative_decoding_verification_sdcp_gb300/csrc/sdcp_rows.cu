@@ -729,6 +729,7 @@ int launch_row_stats(const RowArgs& a, int dtype, int cluster, cudaStream_t stre
     e = cudaLaunchKernelEx(&cfg, row_stats_kernel<__nv_bfloat16>, a);
   else
     e = cudaLaunchKernelEx(&cfg, row_stats_kernel<float>, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? 0 : (int)e;
 }
 

@@ -327,6 +327,7 @@ int launch_sessions(const SessArgs& a, int dtype, int cluster, cudaStream_t stre
     e = cudaLaunchKernelEx(&cfg, session_kernel<__nv_bfloat16>, a);
   else
     e = cudaLaunchKernelEx(&cfg, session_kernel<float>, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? 0 : (int)e;
 }
 

@@ -45,6 +45,11 @@ def _load():
     L.sdcp_verify_batch.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, vp, vp,
                                     vp, vp, sz, vp]
     L.sdcp_verify_batch.restype = ctypes.c_int
+    L.sdcp_verify_rows.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, sz, vp]
+    L.sdcp_verify_rows.restype = ctypes.c_int
+    L.sdcp_verify_sessions.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, vp, vp,
+                                       vp, vp, sz, vp]
+    L.sdcp_verify_sessions.restype = ctypes.c_int
     L.sdcp_row_stats.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, vp, sz, vp]
     L.sdcp_row_stats.restype = ctypes.c_int
     L.sdcp_strerror.argtypes = [ctypes.c_int]
@@ -117,6 +122,28 @@ def sdcp_verify_batch(target_logits, draft_logits, m_offsets, total_drafts, draf
     _check(rc, "sdcp_verify_batch")
 
 
+def sdcp_verify_rows(target_logits, draft_logits, m_offsets, total_drafts, draft_tokens,
+                     params_dev, workspace, B, stream=None):
+    V = target_logits.shape[1]
+    s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
+    rc = lib.sdcp_verify_rows(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits), V,
+                              B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
+                              _ptr(params_dev), _ptr(workspace), workspace.numel(), s)
+    _check(rc, "sdcp_verify_rows")
+
+
+def sdcp_verify_sessions(target_logits, draft_logits, m_offsets, total_drafts, draft_tokens,
+                         params_dev, accepted, n_out, out_tokens, status, workspace, stream=None):
+    V = target_logits.shape[1]
+    B = accepted.shape[0]
+    s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
+    rc = lib.sdcp_verify_sessions(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits),
+                                  V, B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
+                                  _ptr(params_dev), _ptr(accepted), _ptr(n_out), _ptr(out_tokens),
+                                  _ptr(status), _ptr(workspace), workspace.numel(), s)
+    _check(rc, "sdcp_verify_sessions")
+
+
 def sdcp_row_stats(target_logits, draft_logits, m_offsets, total_drafts, draft_tokens, params_dev,
                    stats_out, workspace, stream=None):
     V = target_logits.shape[1]
@@ -144,6 +171,17 @@ class Verifier:
         sdcp_verify_batch(target, draft, m_offsets, self.total, draft_tokens, params_dev,
                           self.accepted, self.n_out, self.out_tokens, self.status,
                           self.workspace, stream)
+        return self.accepted, self.n_out, self.out_tokens, self.status
+
+    def phases(self, target, draft, m_offsets, draft_tokens, params_dev, ev_mid=None):
+        """Phase 1 then phase 2 (identical to __call__), optionally recording ev_mid between."""
+        sdcp_verify_rows(target, draft, m_offsets, self.total, draft_tokens, params_dev,
+                         self.workspace, self.B)
+        if ev_mid is not None:
+            ev_mid.record()
+        sdcp_verify_sessions(target, draft, m_offsets, self.total, draft_tokens, params_dev,
+                             self.accepted, self.n_out, self.out_tokens, self.status,
+                             self.workspace)
         return self.accepted, self.n_out, self.out_tokens, self.status
 
     def row_stats(self, target, draft, m_offsets, draft_tokens, params_dev):
