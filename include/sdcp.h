@@ -72,6 +72,7 @@ extern "C" {
 #define SDCP_E_TOO_LARGE  4  /* V above SDCP_MAX_VOCAB or a row count above INT32_MAX */
 #define SDCP_E_LAUNCH     5  /* a CUDA launch failed (cudaGetLastError after launch) */
 #define SDCP_E_DEVICE     6  /* no usable CUDA device / device query failed */
+#define SDCP_E_SCRATCH_LIMIT 7 /* batch needs more scratch than SDCP_NOALLOC_SCRATCH_BYTES */
 
 /* ---- per-session status (mirrors SDCP Table 2 problem types) ---------------------- */
 #define SDCP_S_OK             0
@@ -203,6 +204,38 @@ int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtyp
                    const int32_t* draft_tokens, const sdcp_session_params* params,
                    sdcp_row_stat* stats_out, void* workspace, size_t workspace_bytes,
                    void* stream);
+
+/*
+ * sdcp_verify_batch for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point: it exists for callers that must not
+ * call cudaMalloc, such as code running inside a CUDA graph being built by someone else,
+ * an allocator-less runtime, or a plugin whose host forbids device allocations.  Instead
+ * of a caller-provided workspace it uses a scratch array of SDCP_NOALLOC_SCRATCH_BYTES that
+ * lives in the library itself (a file-scope __device__ array): every GPU that loads the
+ * library holds that memory until the process exits.  The caller still passes the inputs
+ * and outputs, exactly as for sdcp_verify_batch, and gets identical results.
+ *
+ * Limit: sdcp_workspace_bytes(V, B, total_drafts) must not exceed
+ * SDCP_NOALLOC_SCRATCH_BYTES; larger batches are rejected with SDCP_E_SCRATCH_LIMIT before
+ * anything is launched.  The function calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ * Set-up: the first call on a device looks up the array's device address on the current
+ * device (cudaGetSymbolAddress) and caches it; make that first call outside any stream
+ * capture.  The current device must be the one the stream and the buffers belong to.
+ * Sharing: all calls on a device share the one array and it keeps whatever the last call
+ * left in it; nothing in it needs to start at zero.  Calls whose work overlaps on the GPU
+ * (different streams, or host threads without ordering) race on the array: serialise them.
+ * Returns as sdcp_verify_batch, plus SDCP_E_DEVICE if the device or the array's address
+ * cannot be obtained.
+ */
+#define SDCP_NOALLOC_SCRATCH_BYTES ((size_t)2 << 20)
+int sdcp_verify_batch_noalloc(const void* target_logits, const void* draft_logits, int dtype,
+                              int64_t V, int32_t B, const int32_t* m_offsets,
+                              int64_t total_drafts, const int32_t* draft_tokens,
+                              const sdcp_session_params* params, int32_t* accepted,
+                              int32_t* n_out, int32_t* out_tokens, int32_t* status,
+                              void* stream);
 
 /* Human-readable text for an SDCP_E_* code (static storage, never NULL). */
 const char* sdcp_strerror(int code);

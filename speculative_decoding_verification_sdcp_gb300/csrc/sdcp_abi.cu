@@ -65,6 +65,8 @@ const char* sdcp_strerror(int code) {
     case SDCP_E_TOO_LARGE: return "vocabulary or row count above the supported maximum";
     case SDCP_E_LAUNCH: return "CUDA kernel launch failed";
     case SDCP_E_DEVICE: return "no usable CUDA device";
+    case SDCP_E_SCRATCH_LIMIT:
+      return "batch needs more scratch than the library's no-alloc array (SDCP_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown sdcp error code";
   }
 }

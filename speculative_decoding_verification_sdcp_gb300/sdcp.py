@@ -50,6 +50,9 @@ def _load():
     L.sdcp_verify_sessions.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, vp, vp,
                                        vp, vp, sz, vp]
     L.sdcp_verify_sessions.restype = ctypes.c_int
+    L.sdcp_verify_batch_noalloc.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp,
+                                            vp, vp, vp, vp]
+    L.sdcp_verify_batch_noalloc.restype = ctypes.c_int
     L.sdcp_row_stats.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, vp, sz, vp]
     L.sdcp_row_stats.restype = ctypes.c_int
     L.sdcp_strerror.argtypes = [ctypes.c_int]
@@ -120,6 +123,23 @@ def sdcp_verify_batch(target_logits, draft_logits, m_offsets, total_drafts, draf
                                _ptr(params_dev), _ptr(accepted), _ptr(n_out), _ptr(out_tokens),
                                _ptr(status), _ptr(workspace), workspace.numel(), s)
     _check(rc, "sdcp_verify_batch")
+
+
+NOALLOC_SCRATCH_BYTES = 2 << 20
+
+
+def sdcp_verify_batch_noalloc(target_logits, draft_logits, m_offsets, total_drafts, draft_tokens,
+                              params_dev, accepted, n_out, out_tokens, status, stream=None):
+    """sdcp_verify_batch without a workspace argument: the library's own scratch array is
+    used (for callers that cannot allocate device memory; calls must not overlap)."""
+    V = target_logits.shape[1]
+    B = accepted.shape[0]
+    s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
+    rc = lib.sdcp_verify_batch_noalloc(_ptr(target_logits), _ptr(draft_logits),
+                                       dtype_code(target_logits), V, B, _ptr(m_offsets),
+                                       int(total_drafts), _ptr(draft_tokens), _ptr(params_dev),
+                                       _ptr(accepted), _ptr(n_out), _ptr(out_tokens), _ptr(status), s)
+    _check(rc, "sdcp_verify_batch_noalloc")
 
 
 def sdcp_verify_rows(target_logits, draft_logits, m_offsets, total_drafts, draft_tokens,
