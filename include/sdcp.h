@@ -84,6 +84,8 @@ extern "C" {
                                     m_offsets, or a scored row holding NaN, +inf or only
                                     -inf (no distribution can be formed) */
 #define SDCP_S_Q_UNAVAILABLE  4  /* "sdcp-q-unavailable": Rule 2 without draft logits */
+#define SDCP_S_INTERNAL       5  /* the call gave up a bounded wait on the GPU (a bulk copy
+                                    that never completed); no output of the call is valid */
 
 #define SDCP_MAX_M      64          /* m_max upper bound, SDCP Section 4.1 contract */
 #define SDCP_MAX_VOCAB  (1 << 24)   /* ids and ranks are int32; 16 Mi keeps all sums exact */
@@ -189,8 +191,9 @@ typedef struct sdcp_row_stat {
   float lp_x;
   int32_t argmax;
   int32_t kept;
-  uint32_t thr_key;   /* internal: order key of the last kept token */
-  int32_t thr_id;     /* internal: id bound among tokens sharing that key */
+  uint32_t thr_key;   /* internal: order key of the lowest kept value */
+  int32_t thr_n;      /* internal: how many tokens with that value are kept, the first ones
+                         in id order (INT32_MAX: all) */
   uint32_t flags;
 } sdcp_row_stat;
 

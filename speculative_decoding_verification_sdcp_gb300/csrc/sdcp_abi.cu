@@ -11,22 +11,17 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// CTAs per row cluster: about 32 KB of logits per CTA, 1..8.
-int row_cluster(int64_t V, int dtype) {
-  int64_t bytes = V * (dtype == SDCP_BF16 ? 2 : 4);
-  int64_t c = (bytes + 32767) / 32768;
+// CTAs per session cluster for the draw: enough sessions x CTAs to cover the SMs when the
+// batch is small, never slices under 16 KB of one row; 1..8.
+int session_cluster(int64_t V, int dtype, int32_t B) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const int64_t bytes = V * (dtype == SDCP_BF16 ? 2 : 4);
+  int64_t c = (sms + (int64_t)B - 1) / (B > 0 ? B : 1);
+  const int64_t by_size = (bytes + 16383) / 16384;
+  if (c > by_size) c = by_size;
   return (int)(c < 1 ? 1 : (c > kMaxCluster ? kMaxCluster : c));
-}
-// CTAs per session cluster for the draw, and tiles per CTA (shared-memory prefix array).
-void session_cluster(int64_t V, int dtype, int* cluster, int* tiles_per_cta) {
-  const int64_t tile = (int64_t)kThreads * kEpt;
-  const int64_t nt = (V + tile - 1) / tile;
-  int64_t c = row_cluster(V, dtype);
-  int64_t need = (nt + 1023) / 1024;
-  if (c < need) c = need;
-  if (c > kMaxCluster) c = kMaxCluster;
-  *cluster = (int)c;
-  *tiles_per_cta = (int)((nt + c - 1) / c);
 }
 
 int check_common(const void* target, int dtype, int64_t V, int32_t B, const int32_t* m_offsets,
@@ -43,10 +38,26 @@ int check_common(const void* target, int dtype, int64_t V, int32_t B, const int3
   return SDCP_OK;
 }
 
-size_t stats_bytes(int32_t B, int64_t total) {
-  return align256((size_t)(total + B + total) * sizeof(RowStat));
+int check_workspace(void* workspace, size_t workspace_bytes, int64_t V, int32_t B, int64_t total);
+
+}  // namespace
+}  // namespace sdcp
+
+using namespace sdcp;
+
+extern "C" size_t sdcp_workspace_bytes(int64_t V, int32_t B, int64_t total_drafts) {
+  if (B < 0 || total_drafts < 0 || V < 1 || V > SDCP_MAX_VOCAB) return 0;
+  return kWsHeader + align256((size_t)(total_drafts + B + total_drafts) * sizeof(RowStat));
 }
 
+namespace sdcp {
+namespace {
+int check_workspace(void* workspace, size_t workspace_bytes, int64_t V, int32_t B, int64_t total) {
+  if (!workspace || ((uintptr_t)workspace & 255u) != 0 ||
+      workspace_bytes < sdcp_workspace_bytes(V, B, total))
+    return SDCP_E_WORKSPACE;
+  return SDCP_OK;
+}
 }  // namespace
 }  // namespace sdcp
 
@@ -71,11 +82,6 @@ const char* sdcp_strerror(int code) {
   }
 }
 
-size_t sdcp_workspace_bytes(int64_t V, int32_t B, int64_t total_drafts) {
-  if (B < 0 || total_drafts < 0 || V < 1 || V > SDCP_MAX_VOCAB) return 0;
-  return stats_bytes(B, total_drafts) + 256;
-}
-
 int sdcp_verify_rows(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
                      int32_t B, const int32_t* m_offsets, int64_t total_drafts,
                      const int32_t* draft_tokens, const sdcp_session_params* params,
@@ -84,12 +90,34 @@ int sdcp_verify_rows(const void* target_logits, const void* draft_logits, int dt
                         draft_logits);
   if (rc != SDCP_OK) return rc;
   if (B == 0) return SDCP_OK;
-  if (!workspace || ((uintptr_t)workspace & 255u) != 0 ||
-      workspace_bytes < sdcp_workspace_bytes(V, B, total_drafts))
-    return SDCP_E_WORKSPACE;
+  rc = check_workspace(workspace, workspace_bytes, V, B, total_drafts);
+  if (rc != SDCP_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* err = reinterpret_cast<uint32_t*>(workspace);
+  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return SDCP_E_LAUNCH;
   RowArgs ra{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
-             reinterpret_cast<RowStat*>(workspace), nullptr, 0};
-  if (launch_row_stats(ra, dtype, row_cluster(V, dtype), reinterpret_cast<cudaStream_t>(stream)) != 0)
+             reinterpret_cast<RowStat*>(static_cast<char*>(workspace) + kWsHeader), nullptr, 0, err};
+  if (launch_row_stats(ra, dtype, s) != 0) return SDCP_E_LAUNCH;
+  return SDCP_OK;
+}
+
+static int verify_sessions(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
+                           int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                           const int32_t* draft_tokens, const sdcp_session_params* params,
+                           int32_t* accepted, int32_t* n_out, int32_t* out_tokens, int32_t* status,
+                           void* workspace, size_t workspace_bytes, void* stream, bool pdl) {
+  int rc = check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens, params,
+                        draft_logits);
+  if (rc != SDCP_OK) return rc;
+  if (B == 0) return SDCP_OK;
+  if (!accepted || !n_out || !out_tokens || !status) return SDCP_E_INVALID;
+  rc = check_workspace(workspace, workspace_bytes, V, B, total_drafts);
+  if (rc != SDCP_OK) return rc;
+  const char* ws = static_cast<const char*>(workspace);
+  SessArgs sa{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
+              reinterpret_cast<const RowStat*>(ws + kWsHeader), accepted, n_out, out_tokens, status,
+              reinterpret_cast<const uint32_t*>(ws)};
+  if (launch_sessions(sa, dtype, session_cluster(V, dtype, B), pdl, reinterpret_cast<cudaStream_t>(stream)) != 0)
     return SDCP_E_LAUNCH;
   return SDCP_OK;
 }
@@ -99,20 +127,9 @@ int sdcp_verify_sessions(const void* target_logits, const void* draft_logits, in
                          const int32_t* draft_tokens, const sdcp_session_params* params,
                          int32_t* accepted, int32_t* n_out, int32_t* out_tokens, int32_t* status,
                          void* workspace, size_t workspace_bytes, void* stream) {
-  int rc = check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens, params,
-                        draft_logits);
-  if (rc != SDCP_OK) return rc;
-  if (B == 0) return SDCP_OK;
-  if (!accepted || !n_out || !out_tokens || !status) return SDCP_E_INVALID;
-  if (!workspace || ((uintptr_t)workspace & 255u) != 0 ||
-      workspace_bytes < sdcp_workspace_bytes(V, B, total_drafts))
-    return SDCP_E_WORKSPACE;
-  int c2, tiles;
-  session_cluster(V, dtype, &c2, &tiles);
-  SessArgs sa{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
-              reinterpret_cast<const RowStat*>(workspace), accepted, n_out, out_tokens, status, tiles};
-  if (launch_sessions(sa, dtype, c2, reinterpret_cast<cudaStream_t>(stream)) != 0) return SDCP_E_LAUNCH;
-  return SDCP_OK;
+  return verify_sessions(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
+                         draft_tokens, params, accepted, n_out, out_tokens, status, workspace,
+                         workspace_bytes, stream, false);
 }
 
 int sdcp_verify_batch(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
@@ -128,9 +145,10 @@ int sdcp_verify_batch(const void* target_logits, const void* draft_logits, int d
   int rc = sdcp_verify_rows(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
                             draft_tokens, params, workspace, workspace_bytes, stream);
   if (rc != SDCP_OK || B == 0) return rc;
-  return sdcp_verify_sessions(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
-                              draft_tokens, params, accepted, n_out, out_tokens, status, workspace,
-                              workspace_bytes, stream);
+  // phase 2 is a programmatic dependent of phase 1: its launch overlaps phase 1's tail
+  return verify_sessions(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
+                         draft_tokens, params, accepted, n_out, out_tokens, status, workspace,
+                         workspace_bytes, stream, true);
 }
 
 int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
@@ -144,14 +162,14 @@ int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtyp
   if (B == 0) return SDCP_OK;
   if (!stats_out) return SDCP_E_INVALID;
   if (total_drafts > 0 && !draft_logits) return SDCP_E_INVALID;
-  if (!workspace || ((uintptr_t)workspace & 255u) != 0 ||
-      workspace_bytes < sdcp_workspace_bytes(V, B, total_drafts))
-    return SDCP_E_WORKSPACE;
+  rc = check_workspace(workspace, workspace_bytes, V, B, total_drafts);
+  if (rc != SDCP_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* err = reinterpret_cast<uint32_t*>(workspace);
+  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return SDCP_E_LAUNCH;
   RowArgs ra{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
-             reinterpret_cast<RowStat*>(workspace), stats_out, 1};
-  if (launch_row_stats(ra, dtype, row_cluster(V, dtype), s) != 0) return SDCP_E_LAUNCH;
-  if (cudaGetLastError() != cudaSuccess) return SDCP_E_LAUNCH;
+             reinterpret_cast<RowStat*>(static_cast<char*>(workspace) + kWsHeader), stats_out, 1, err};
+  if (launch_row_stats(ra, dtype, s) != 0) return SDCP_E_LAUNCH;
   return SDCP_OK;
 }
 

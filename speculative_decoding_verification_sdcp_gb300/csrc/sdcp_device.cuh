@@ -7,7 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/sdcp.h"
+#include "sdcp.h"
 
 namespace sdcp {
 
@@ -26,8 +26,8 @@ struct RowStat {
   float s;           // sum over the kept set of exp((l - lmax) * 1000/T); 1 at T = 0
   float dlx;         // l[x] - lmax for the row's draft token (-inf: x has a -inf logit)
   int32_t argmax;    // smallest id of the largest logit (rows that need it)
-  uint32_t thr_key;  // kept iff key > thr_key, or key == thr_key and id <= thr_id
-  int32_t thr_id;
+  uint32_t thr_key;  // kept: key > thr_key, or key == thr_key and among the first thr_n
+  int32_t thr_n;     //   tokens with that key in id order (INT_MAX: all of them)
   int32_t kept;      // size of the kept set
   uint32_t flags;    // SDCP_ROW_* plus kRowHasX
 };
@@ -48,6 +48,7 @@ struct RowArgs {
   RowStat* stats;             // [total + B + total]: target rows, then draft rows
   sdcp_row_stat* pub;         // optional public copy (statistics mode)
   int stats_mode;             // 1: every row gets the full statistics
+  uint32_t* error;            // workspace word: non-zero if a bounded wait gave up
 };
 
 // Arguments of the session kernel (phase 2).
@@ -65,11 +66,14 @@ struct SessArgs {
   int32_t* n_out;
   int32_t* out_tokens;
   int32_t* status;
-  int max_tiles_per_cta;      // length of the per-CTA tile prefix array (dynamic smem)
+  const uint32_t* error;      // the row kernel's error word
 };
 
-int launch_row_stats(const RowArgs& a, int dtype, int cluster, cudaStream_t stream);
-int launch_sessions(const SessArgs& a, int dtype, int cluster, cudaStream_t stream);
+// Workspace: [0, 256) error word, then one RowStat per scored row.
+constexpr size_t kWsHeader = 256;
+
+int launch_row_stats(const RowArgs& a, int dtype, cudaStream_t stream);
+int launch_sessions(const SessArgs& a, int dtype, int cluster, bool pdl, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------------
 // Order key of a binary32 bit pattern: unsigned order of keys = numeric order of the
@@ -369,6 +373,152 @@ __device__ __forceinline__ int32_t find_session(const int32_t* __restrict__ m_of
     hi = nhi < hi ? nhi : hi;
   }
   return (int32_t)lo;
+}
+
+// ---------------------------------------------------------------------------------
+// mbarrier and bulk-copy (TMA) primitives, PTX ISA 8.x, shared::cta addresses.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }"
+               ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+               : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return done != 0;
+}
+// Bounded wait for the phase of `parity` to complete: false after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
+  for (long long it = 0; it < limit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// Global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+// Named barrier for a subset of the block (thread count a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Programmatic dependent launch controls (no-ops when the launch did not enable them).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------
+// Reductions over a group of warps 0..nw-1 that share a named barrier (fixed order).
+// scratch needs 2 * 32 + 2 entries.
+// ---------------------------------------------------------------------------------
+struct Group {
+  int nthreads;
+  int bar;
+  __device__ __forceinline__ void sync() const { named_sync(bar, nthreads); }
+  __device__ __forceinline__ int nwarps() const { return nthreads >> 5; }
+};
+__device__ __forceinline__ float group_sum(const Group& g, float v, float* scratch) {
+  v = warp_reduce(v, [](float a, float b) { return a + b; });
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  g.sync();
+  if (l == 0) scratch[w] = v;
+  g.sync();
+  float r = 0.f;
+  for (int i = 0; i < g.nwarps(); ++i) r += scratch[i];
+  return r;
+}
+__device__ __forceinline__ long long group_sum_ll(const Group& g, long long v, long long* scratch) {
+  v = warp_sum_ll(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  g.sync();
+  if (l == 0) scratch[w] = v;
+  g.sync();
+  long long r = 0;
+  for (int i = 0; i < g.nwarps(); ++i) r += scratch[i];
+  return r;
+}
+__device__ __forceinline__ int64_t group_max_i64(const Group& g, int64_t v, long long* scratch) {
+  v = warp_max_i64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  g.sync();
+  if (l == 0) scratch[w] = v;
+  g.sync();
+  int64_t r = INT64_MIN;
+  for (int i = 0; i < g.nwarps(); ++i) r = max(r, (int64_t)scratch[i]);
+  return r;
+}
+__device__ __forceinline__ int64_t group_min_i64(const Group& g, int64_t v, long long* scratch) {
+  v = warp_min_i64(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  g.sync();
+  if (l == 0) scratch[w] = v;
+  g.sync();
+  int64_t r = INT64_MAX;
+  for (int i = 0; i < g.nwarps(); ++i) r = min(r, (int64_t)scratch[i]);
+  return r;
+}
+// Exclusive scans over the group (fixed association); *total = group sum.
+__device__ __forceinline__ float group_excl_scan(const Group& g, float v, float* scratch, float* total) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  float incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    float t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (l >= o) incl += t;
+  }
+  float ex = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (l == 0) ex = 0.f;
+  g.sync();
+  if (l == 31) scratch[w] = incl;
+  g.sync();
+  float base = 0.f, tot = 0.f;
+  for (int i = 0; i < g.nwarps(); ++i) {
+    if (i == w) base = tot;
+    tot += scratch[i];
+  }
+  *total = tot;
+  return base + ex;
+}
+__device__ __forceinline__ long long group_excl_scan_ll(const Group& g, long long v, long long* scratch,
+                                                        long long* total) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (l >= o) incl += t;
+  }
+  long long ex = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (l == 0) ex = 0;
+  g.sync();
+  if (l == 31) scratch[w] = incl;
+  g.sync();
+  long long base = 0, tot = 0;
+  for (int i = 0; i < g.nwarps(); ++i) {
+    if (i == w) base = tot;
+    tot += scratch[i];
+  }
+  *total = tot;
+  return base + ex;
 }
 
 }  // namespace sdcp

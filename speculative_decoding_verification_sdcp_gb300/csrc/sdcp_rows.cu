@@ -2,692 +2,757 @@
 // profile (SDCP draft draft-li-mlc-inference-acceleration-00, Section 4.1: temperature,
 // then top-k, then top-p; temperature 0 selects the argmax, ties to the smallest id).
 //
-// One thread-block cluster of C CTAs per logits row (C = 1..8).  CTA r of the cluster
-// streams slice r of the row from HBM once (16-byte non-allocating loads) and keeps, per
-// thread, the running maximum and the sum of exp relative to it (online softmax), or the
-// order-key maximum with its smallest id when the row needs an argmax.  The CTAs merge
-// their partials in rank order through distributed shared memory, so every result is
-// independent of scheduling.
+// A persistent kernel, two CTAs per SM.  In each CTA one producer warp streams the rows the
+// CTA owns (rows blockIdx.x, blockIdx.x + gridDim.x, ...) from HBM into a ring of three
+// 32 KB shared-memory stages with bulk copies (TMA) that complete on mbarriers; eight
+// consumer warps reduce each stage as it lands (eight 16-byte vectors per thread) and hand
+// it back.  The HBM stream therefore does not wait for the per-row work (reductions,
+// thresholds, the statistics record): every logits byte is read from HBM once, and up to
+// 64 KB per CTA are in flight.
 //
-// Top-k / top-p on bf16 rows: one more pass over the row (it is still in L2) builds an
-// exact-value histogram of the 2048 bf16 values just below the row maximum (integer
-// shared-memory atomics: deterministic).  Because all tokens that share a bf16 value have
-// the same probability, the mass of a bin is count * exp(value - max): the k-th token and
-// the top-p crossing come out of one block scan over the bins.  A tie at the cut value is
-// broken by id with a cluster-wide list of the tied ids.  Rows the window cannot decide
-// (fp32 logits with filters, or a distribution too flat for 2048 bins) take a generic
-// bisection over the order-key space on the cluster's rank 0.
+// Per row the consumers keep, per thread, the running maximum, its smallest id when the row
+// needs an argmax, and the sum of exp relative to it (online softmax) when it needs one;
+// warps merge in a fixed order, so every result is independent of scheduling.
+//
+// Top-k / top-p on bf16 rows: an exact-value histogram of the bf16 values within Dz nats
+// below the row maximum (8 for top-k, 11 for top-p, then twice that, then the 2048 values)
+// is built from a second read of the row (it was just streamed and sits in L2); only
+// vectors whose maximum reaches the window are looked at element by element (integer
+// shared-memory atomics: deterministic).  All tokens that share a bf16 value have the same
+// probability, so the mass of a bin is count * exp(v - max): the k-th token and the top-p
+// crossing come out of one scan over the bins.  A tie at the cut value is broken by id
+// after one more pass that collects the ids holding that value.  Rows no window decides
+// (fp32 logits with a filter, or a nucleus deeper than 2048 values) take a generic
+// bisection over the order-key space.
 #include "sdcp_device.cuh"
 
 namespace sdcp {
 
+constexpr int kConsWarps = 8;
+constexpr int kCons = kConsWarps * 32;  // consumer threads
+constexpr int kProducerWarp = kConsWarps;
+constexpr int kRowThreads = kCons + 32;
+constexpr int kStages = 3;
+constexpr int kChunk = 32768;            // bytes per ring stage (8 vectors per consumer thread)
+constexpr int kConsBar = 1;              // named barrier of the consumer warps
+constexpr long long kWaitPolls = 1ll << 22;
+constexpr int kRowCtasPerSm = 2;
 
-// What one CTA publishes for its cluster after the streaming pass.
-struct Partial {
-  float fm;        // running maximum used as the reference of s
-  float s;         // sum of exp((l - fm) * scale) over the slice
-  uint32_t kmax;   // largest order key
-  uint32_t kmin;   // smallest order key
-  long long amax;  // smallest id holding kmax (LLONG_MAX: none)
-  int bad;         // NaN seen (sum mode)
-  int pad;
+struct RowPlan {
+  long long row_id;  // < 0: end of the CTA's work
+  int b;
+  int nchunks;
 };
 
-// Decision of rank 0 after the window histogram, read by the cluster.
-struct Decision {
-  int use_fallback;
-  int need_tie;
-  uint32_t tie_key16;
-  int tie_n;        // 1-based rank (id order) of the last kept token among the tied ones
-  uint32_t thr_key;
-  int kept;
-  float s_kept;
-  int pad;
-};
-
-struct __align__(16) RowSmem {
-  Partial part;
-  Decision dec;
+struct RowShared {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  RowPlan plan[kStages];
+  volatile int abort;
+  int pad0;
+  // per-warp partials and the merged row result
+  float w_fm[32], w_s[32];
+  long long w_amax[32];
+  float r_lmax, r_s;
+  long long r_amax;
+  float fscr[2 * 32 + 4];
+  long long lscr[2 * 32 + 4];
+  // window histogram and the list of the window's tokens (value key, id)
   uint32_t hist[kWindowBins];
-  int tie_count;
-  int tie_ids[kTieListCap];
-  float fscr[3 * kWarps + 4];
-  long long lscr[3 * kWarps + 4];
-  // broadcast slots of rank 0's scans
-  int b_dk, b_tk, b_dp, b_np, b_found;
-  float b_sk1, b_massbefore_p, b_s_kept;
-  int b_countbefore_p;
-  int b_tie_id;
+  // window built while the row streams: anchored on the maximum of its first stage
+  float win_lo;            // lowest value in the window
+  uint32_t win_top16;      // bin i holds the bf16 value key win_top16 - i
+  int win_on, win_over;    // window in use; a token above the top was seen
+  int b_dk, b_tk, b_dp, b_np, b_found, b_cbefore;
+  float b_mbefore;
 };
 
 // --------------------------------------------------------------------------------------
-// Streaming pass over a set of elements.
+// Per-thread accumulation.  Every row keeps the running maximum fm (max.NaN, so a NaN
+// poisons it); ARGMAX rows also keep the smallest id holding fm (float equality, so -0 and
+// +0 tie and go to the smaller id); SUM rows keep s = sum exp((l - fm) * 1000/T), the sum
+// being rescaled whenever fm grows (online softmax).
 // --------------------------------------------------------------------------------------
 struct ThreadAcc {
-  float fm, s;
-  uint32_t kmax, kmin;
+  float fm, fmc, s;  // fmc = fm * c
   long long amax;
-  int bad;
+  __device__ __forceinline__ void reset() { fm = -INFINITY; fmc = -INFINITY; s = 0.f; amax = LLONG_MAX; }
 };
 
-// FMODE: 0 no float statistics, 1 running maximum only, 2 maximum and online sum.
-template <bool KEYS, int FMODE>
+template <bool ARGMAX, bool SUM>
 __device__ __forceinline__ void acc_element(ThreadAcc& a, uint32_t bits, long long id, float c) {
-  if (KEYS) {
-    uint32_t k = order_key(bits);
-    if (k > a.kmax) { a.kmax = k; a.amax = id; }
-    a.kmin = min(a.kmin, k);
+  const float v = __uint_as_float(bits);
+  const float nm = fmax_nan(a.fm, v);
+  if (!(nm == a.fm)) {  // grew, or became NaN
+    if (SUM) a.s = (a.fm == -INFINITY) ? 0.f : a.s * ex2(a.fmc - nm * c);
+    if (ARGMAX) a.amax = id;
+    a.fm = nm;
+    a.fmc = nm * c;
   }
-  if (FMODE >= 1) {
-    float v = __uint_as_float(bits);
-    if (v != v) a.bad = 1;
-    if (v > a.fm) {
-      if (FMODE == 2) a.s = a.s * ex2((a.fm - v) * c);
-      a.fm = v;
-    }
-    if (FMODE == 2 && a.fm != -INFINITY) a.s += ex2((v - a.fm) * c);
-  }
+  if (SUM && a.fm != -INFINITY) a.s += ex2(fmaf(v, c, -a.fmc));
 }
 
-template <typename T, bool KEYS, int FMODE>
+// Maximum of one 16-byte vector, NaN-propagating (bf16: three packed bf16x2 max.NaN).
+__device__ __forceinline__ float vec_max(const uint4& q, float) {
+  float m0 = fmax_nan(__uint_as_float(q.x), __uint_as_float(q.y));
+  float m1 = fmax_nan(__uint_as_float(q.z), __uint_as_float(q.w));
+  return fmax_nan(m0, m1);
+}
+__device__ __forceinline__ float vec_max(const uint4& q, __nv_bfloat16) {
+  const __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&q.x),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&q.y));
+  const __nv_bfloat162 b = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&q.z),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&q.w));
+  const __nv_bfloat162 ab = __hmax2_nan(a, b);
+  const uint32_t m = *reinterpret_cast<const uint32_t*>(&ab);
+  return fmax_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
+template <typename T, bool ARGMAX, bool SUM>
 __device__ __forceinline__ void acc_vector(ThreadAcc& a, const uint4& q, long long id0, float c) {
   constexpr int E = Elem<T>::kPerVec;
   uint32_t b[E];
   Elem<T>::unpack(q, b);
-  if (KEYS) {
-    uint32_t k[E];
-    uint32_t vmax = 0, vmin = 0xFFFFFFFFu;
+  float v[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) { k[e] = order_key(b[e]); vmax = max(vmax, k[e]); vmin = min(vmin, k[e]); }
-    a.kmin = min(a.kmin, vmin);
-    if (vmax > a.kmax) {
+  for (int e = 0; e < E; ++e) v[e] = __uint_as_float(b[e]);
+  const float vm = vec_max(q, T());
+  const float nm = fmax_nan(a.fm, vm);
+  if (!(nm == a.fm)) {  // the maximum grew (or a NaN arrived): rare after the first vectors
+    if (SUM) a.s = (a.fm == -INFINITY) ? 0.f : a.s * ex2(a.fmc - nm * c);
+    if (ARGMAX) {
       int first = E - 1;
 #pragma unroll
-      for (int e = E - 1; e >= 0; --e) if (k[e] == vmax) first = e;
-      a.kmax = vmax;
+      for (int e = E - 1; e >= 0; --e) if (v[e] == nm) first = e;
       a.amax = id0 + first;
     }
+    a.fm = nm;
+    a.fmc = nm * c;
   }
-  if (FMODE >= 1) {
-    float v[E];
-    float vm = -INFINITY;
+  if (SUM && a.fm != -INFINITY) {
+    float t = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) { v[e] = __uint_as_float(b[e]); vm = fmax_nan(vm, v[e]); }
-    if (vm != vm) a.bad = 1;
-    if (vm > a.fm) {
-      if (FMODE == 2) a.s = a.s * ex2((a.fm - vm) * c);
-      a.fm = vm;
-    }
-    if (FMODE == 2 && a.fm != -INFINITY) {
-      float t = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) t += ex2((v[e] - a.fm) * c);
-      a.s += t;
-    }
+    for (int e = 0; e < E; ++e) t += ex2(fmaf(v[e], c, -a.fmc));
+    a.s += t;
   }
 }
 
-// Elements [e_lo, e_hi) of the row, split as head / vectors / tail.
-template <typename T, bool KEYS, int FMODE>
-__device__ void stream_slice(const T* __restrict__ row, const RowLayout& L, int64_t vec_lo,
-                             int64_t vec_hi, bool head, bool tail, int64_t V, float c,
-                             ThreadAcc& a) {
+// Vectors [0, nv) of one ring stage; vector v is element id0 + v * E of the row.
+template <typename T, bool ARGMAX, bool SUM>
+__device__ __forceinline__ void acc_stage(ThreadAcc& a, const uint4* sv, int nv, long long id0, float c) {
   constexpr int E = Elem<T>::kPerVec;
-  const int tid = threadIdx.x;
-  if (head) {
-    for (int64_t j = tid; j < L.head; j += kThreads) acc_element<KEYS, FMODE>(a, load_bits(row, j), j, c);
-  }
-  const uint4* vp = reinterpret_cast<const uint4*>(row + L.head);
-  constexpr int U = 4;
-  int64_t v = vec_lo + tid;
-  for (; v + (U - 1) * kThreads < vec_hi; v += U * kThreads) {
-    uint4 q[U];
+  int v = threadIdx.x;
+  for (; v + 3 * kCons < nv; v += 4 * kCons) {
+    uint4 q[4];
 #pragma unroll
-    for (int u = 0; u < U; ++u) q[u] = ld_stream(vp + v + u * kThreads);
+    for (int u = 0; u < 4; ++u) q[u] = sv[v + u * kCons];
 #pragma unroll
-    for (int u = 0; u < U; ++u) acc_vector<T, KEYS, FMODE>(a, q[u], L.head + (v + u * kThreads) * E, c);
+    for (int u = 0; u < 4; ++u) acc_vector<T, ARGMAX, SUM>(a, q[u], id0 + (long long)(v + u * kCons) * E, c);
   }
-  for (; v < vec_hi; v += kThreads) acc_vector<T, KEYS, FMODE>(a, ld_stream(vp + v), L.head + v * E, c);
-  if (tail) {
-    for (int64_t j = L.tail0 + tid; j < V; j += kThreads) acc_element<KEYS, FMODE>(a, load_bits(row, j), j, c);
-  }
+  for (; v < nv; v += kCons) acc_vector<T, ARGMAX, SUM>(a, sv[v], id0 + (long long)v * E, c);
 }
 
-// --------------------------------------------------------------------------------------
-// Generic element visitor over a slice (used by the window, tie and fallback passes).
-// --------------------------------------------------------------------------------------
-template <typename T, typename F>
-__device__ __forceinline__ void visit_slice(const T* __restrict__ row, const RowLayout& L,
-                                            int64_t vec_lo, int64_t vec_hi, bool head, bool tail,
-                                            int64_t V, F f) {
-  constexpr int E = Elem<T>::kPerVec;
-  const int tid = threadIdx.x;
-  if (head)
-    for (int64_t j = tid; j < L.head; j += kThreads) f(load_bits(row, j), j);
-  const uint4* vp = reinterpret_cast<const uint4*>(row + L.head);
-  for (int64_t v = vec_lo + tid; v < vec_hi; v += kThreads) {
-    uint4 q = __ldg(vp + v);
-    uint32_t b[E];
-    Elem<T>::unpack(q, b);
-    long long id0 = L.head + v * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) f(b[e], id0 + e);
-  }
-  if (tail)
-    for (int64_t j = L.tail0 + tid; j < V; j += kThreads) f(load_bits(row, j), j);
+template <typename T, bool ARGMAX, bool SUM>
+__device__ __forceinline__ void acc_scalars(ThreadAcc& a, const T* row, const RowLayout& L, int64_t V, float c) {
+  for (int64_t j = threadIdx.x; j < L.head; j += kCons) acc_element<ARGMAX, SUM>(a, load_bits(row, j), j, c);
+  for (int64_t j = L.tail0 + threadIdx.x; j < V; j += kCons) acc_element<ARGMAX, SUM>(a, load_bits(row, j), j, c);
 }
 
-// Whole-row generic passes run by one CTA (the fallback).
+// Row modes: which statistics a row needs.
+enum RowMode { kModeMax = 0, kModeArgmax = 1, kModeSum = 2, kModeArgmaxSum = 3 };
+
 template <typename T>
-struct WholeRow {
-  const T* row;
-  RowLayout L;
-  int64_t V;
-  template <typename F>
-  __device__ __forceinline__ void visit(F f) const { visit_slice<T>(row, L, 0, L.nvec, true, true, V, f); }
+__device__ __forceinline__ void acc_stage_mode(int mode, ThreadAcc& a, const uint4* sv, int nv,
+                                               long long id0, float c) {
+  switch (mode) {
+    case kModeMax: acc_stage<T, false, false>(a, sv, nv, id0, c); break;
+    case kModeArgmax: acc_stage<T, true, false>(a, sv, nv, id0, c); break;
+    case kModeSum: acc_stage<T, false, true>(a, sv, nv, id0, c); break;
+    default: acc_stage<T, true, true>(a, sv, nv, id0, c); break;
+  }
+}
+template <typename T>
+__device__ __forceinline__ void acc_scalars_mode(int mode, ThreadAcc& a, const T* row, const RowLayout& L,
+                                                 int64_t V, float c) {
+  switch (mode) {
+    case kModeMax: acc_scalars<T, false, false>(a, row, L, V, c); break;
+    case kModeArgmax: acc_scalars<T, true, false>(a, row, L, V, c); break;
+    case kModeSum: acc_scalars<T, false, true>(a, row, L, V, c); break;
+    default: acc_scalars<T, true, true>(a, row, L, V, c); break;
+  }
+}
+
+// --------------------------------------------------------------------------------------
+// What a row needs, from its session (identical for the producer and the consumers).
+// --------------------------------------------------------------------------------------
+struct RowCtx {
+  bool skip, is_target, has_x, one_hot, topk, topp, need_keys, need_sum, need_max, window;
+  int b;
+  long long tok_idx;
+  double scale_d;
+  float c;
+  sdcp_session_params P;
+  int mode;
 };
 
-// Id (1-based rank n in id order) among the tokens whose key satisfies pred, by one CTA:
-// each thread owns a contiguous chunk of ids, counts, scans, and the owner walks.
-template <typename T, typename P>
-__device__ long long nth_matching_id(const WholeRow<T>& R, long long n, P pred, long long* lscr) {
-  const int tid = threadIdx.x;
-  int64_t chunk = (R.V + kThreads - 1) / kThreads;
-  int64_t j0 = (int64_t)tid * chunk, j1 = min(R.V, j0 + chunk);
-  long long cnt = 0;
-  for (int64_t j = j0; j < j1; ++j) cnt += pred(load_bits(R.row, j), j) ? 1 : 0;
-  long long tot;
-  long long excl = block_exclusive_scan_ll(cnt, lscr, &tot);
-  long long found = LLONG_MAX;
-  if (excl < n && n <= excl + cnt) {
-    long long c = excl;
-    for (int64_t j = j0; j < j1; ++j) {
-      if (pred(load_bits(R.row, j), j)) {
-        if (++c == n) { found = j; break; }
-      }
-    }
-  }
-  return block_min_i64(found, lscr);
-}
-
-// --------------------------------------------------------------------------------------
-// The row kernel.
-// --------------------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(kThreads) row_stats_kernel(RowArgs A) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const unsigned C = cluster.num_blocks();
-  const unsigned rank = cluster.block_rank();
-  const int tid = threadIdx.x;
-  const int64_t row_id = (int64_t)blockIdx.x / C;
-  const int64_t R_T = A.total + A.B;
-  const bool is_target = row_id < R_T;
-
-  __shared__ RowSmem sm;
-  __shared__ int s_b;
-
-  // ---- which session / position this row belongs to ------------------------------
-  if (tid < 32) {
-    int32_t b = find_session(A.m_offsets, A.B, is_target ? row_id : row_id - R_T, is_target);
-    if (tid == 0) s_b = b;
-  }
-  __syncthreads();
-  const int32_t b = s_b;
-  const sdcp_session_params P = A.params[b];
-  const int64_t off0 = A.m_offsets[b], off1 = A.m_offsets[b + 1];
-  const int64_t M = off1 - off0;
-  const int64_t pos = is_target ? row_id - off0 - b : (row_id - R_T) - off0;
-  // draft token carried by the row: target row i < M and draft row i carry x[i]
-  const int64_t tok_idx = is_target ? row_id - b : row_id - R_T;
-  const bool has_x = (pos >= 0 && pos < M && tok_idx >= 0 && tok_idx < A.total);
-
-  const bool params_ok = (P.top_p_milli <= 1000u);
-  const bool session_ok = params_ok && (P.rule_id == 1u || P.rule_id == 2u) && M >= 1 &&
+__device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, int b, bool bf16) {
+  RowCtx x;
+  const long long R_T = A.total + A.B;
+  x.is_target = row_id < R_T;
+  x.b = b;
+  x.P = A.params[b];
+  const long long off0 = A.m_offsets[b], off1 = A.m_offsets[b + 1];
+  const long long M = off1 - off0;
+  const long long pos = x.is_target ? row_id - off0 - b : (row_id - R_T) - off0;
+  x.tok_idx = x.is_target ? row_id - b : row_id - R_T;
+  x.has_x = (pos >= 0 && pos < M && x.tok_idx >= 0 && x.tok_idx < A.total);
+  const bool params_ok = (x.P.top_p_milli <= 1000u);
+  const bool session_ok = params_ok && (x.P.rule_id == 1u || x.P.rule_id == 2u) && M >= 1 &&
                           M <= SDCP_MAX_M && off0 >= 0 && off1 <= A.total;
-  bool skip;
   bool want_argmax, want_profile;
   if (A.stats_mode) {
-    skip = !params_ok;
+    x.skip = !params_ok;
     want_argmax = true;
     want_profile = true;
   } else {
-    const bool rule2 = (P.rule_id == 2u);
-    skip = !session_ok || (!is_target && !rule2) || (!is_target && A.draft == nullptr);
-    want_argmax = !rule2 || P.temperature_milli == 0u;
-    want_profile = rule2 && P.temperature_milli != 0u;
+    const bool rule2 = (x.P.rule_id == 2u);
+    x.skip = !session_ok || (!x.is_target && !rule2) || (!x.is_target && A.draft == nullptr);
+    want_argmax = !rule2 || x.P.temperature_milli == 0u;
+    want_profile = rule2 && x.P.temperature_milli != 0u;
   }
-  RowStat* out = A.stats + row_id;
-  if (skip) {
-    if (rank == 0 && tid == 0) {
-      RowStat r{};
-      r.flags = SDCP_ROW_SKIPPED;
-      *out = r;
-      if (A.pub) {
-        sdcp_row_stat q{};
-        q.flags = SDCP_ROW_SKIPPED;
-        q.lp_x = __int_as_float(0x7FC00000);
-        A.pub[row_id] = q;
+  const uint32_t tm = x.P.temperature_milli;
+  x.one_hot = (tm == 0u);
+  x.scale_d = x.one_hot ? 0.0 : 1000.0 / (double)tm;
+  x.c = (float)(x.scale_d * 1.4426950408889634);  // log2(e) * 1000/T
+  x.topk = !x.one_hot && want_profile && x.P.top_k != 0u && (int64_t)x.P.top_k < A.V;
+  x.topp = !x.one_hot && want_profile && x.P.top_p_milli < 1000u;
+  x.need_keys = want_argmax || x.one_hot;  // the argmax is needed
+  x.need_sum = want_profile && !x.one_hot && !x.topk;
+  x.need_max = want_profile && !x.one_hot;
+  x.mode = x.need_keys ? (x.need_sum ? kModeArgmaxSum : kModeArgmax) : (x.need_sum ? kModeSum : kModeMax);
+  x.window = (x.topk || x.topp) && bf16;
+  return x;
+}
+
+template <typename T>
+__device__ __forceinline__ const T* row_ptr(const RowArgs& A, long long row_id) {
+  const long long R_T = A.total + A.B;
+  const T* base = reinterpret_cast<const T*>(row_id < R_T ? A.target : A.draft);
+  return base + (row_id < R_T ? row_id : row_id - R_T) * A.V;
+}
+
+__device__ __forceinline__ void write_skipped(const RowArgs& A, long long row_id) {
+  RowStat r{};
+  r.flags = SDCP_ROW_SKIPPED;
+  A.stats[row_id] = r;
+  if (A.pub) {
+    sdcp_row_stat q{};
+    q.flags = SDCP_ROW_SKIPPED;
+    q.lp_x = __int_as_float(0x7FC00000);
+    A.pub[row_id] = q;
+  }
+}
+
+// --------------------------------------------------------------------------------------
+// Whole-row passes by the consumer group (second reads hit L2).
+// --------------------------------------------------------------------------------------
+template <typename T, typename F>
+__device__ __forceinline__ void visit_row(const T* __restrict__ row, const RowLayout& L, int64_t V, F f) {
+  constexpr int E = Elem<T>::kPerVec;
+  const int t = threadIdx.x;
+  for (int64_t j = t; j < L.head; j += kCons) f(load_bits(row, j), j);
+  const uint4* vp = reinterpret_cast<const uint4*>(row + L.head);
+  int64_t v = t;
+  for (; v + kCons < L.nvec; v += 2 * kCons) {
+    const uint4 q0 = __ldg(vp + v), q1 = __ldg(vp + v + kCons);
+    uint32_t b0[E], b1[E];
+    Elem<T>::unpack(q0, b0);
+    Elem<T>::unpack(q1, b1);
+    const long long i0 = L.head + v * E, i1 = L.head + (v + kCons) * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) f(b0[e], i0 + e);
+#pragma unroll
+    for (int e = 0; e < E; ++e) f(b1[e], i1 + e);
+  }
+  if (v < L.nvec) {
+    const uint4 q = __ldg(vp + v);
+    uint32_t b[E];
+    Elem<T>::unpack(q, b);
+    const long long i0 = L.head + v * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) f(b[e], i0 + e);
+  }
+  for (int64_t j = L.tail0 + t; j < V; j += kCons) f(load_bits(row, j), j);
+}
+
+// Coalesced pass over a row from global memory (L2) by the consumer group, eight 16-byte
+// loads in flight per thread.  f(bits[E], id of bits[0], count of valid elements).
+template <typename T, typename F>
+__device__ __forceinline__ void scan_row(const T* __restrict__ row, const RowLayout& L, int64_t V, F f) {
+  constexpr int E = Elem<T>::kPerVec;
+  constexpr int U = 8;
+  const int t = threadIdx.x;
+  for (int64_t j = t; j < L.head; j += kCons) {
+    uint32_t b[E];
+    b[0] = load_bits(row, j);
+#pragma unroll
+    for (int e = 1; e < E; ++e) b[e] = 0xFF800000u;
+    f(b, j, 1);
+  }
+  const uint4* vp = reinterpret_cast<const uint4*>(row + L.head);
+  for (int64_t v0 = t; v0 < L.nvec; v0 += (int64_t)U * kCons) {
+    uint4 q[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = v0 + (int64_t)u * kCons;
+      q[u] = (v < L.nvec) ? __ldg(vp + v) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = v0 + (int64_t)u * kCons;
+      if (v >= L.nvec) break;
+      uint32_t b[E];
+      Elem<T>::unpack(q[u], b);
+      f(b, L.head + v * E, E);
+    }
+  }
+  for (int64_t j = L.tail0 + t; j < V; j += kCons) {
+    uint32_t b[E];
+    b[0] = load_bits(row, j);
+#pragma unroll
+    for (int e = 1; e < E; ++e) b[e] = 0xFF800000u;
+    f(b, j, 1);
+  }
+}
+
+// Id of the n-th (1-based, id order) token satisfying pred: each consumer thread owns a
+// contiguous run of ids, counts, scans, and the owner walks its run again.
+template <typename T, typename P>
+__device__ long long nth_matching_id(const Group& g, const T* row, int64_t V, long long n, P pred,
+                                     long long* lscr) {
+  const int t = threadIdx.x;
+  const int64_t chunk = (V + kCons - 1) / kCons;
+  const int64_t j0 = (int64_t)t * chunk, j1 = min(V, j0 + chunk);
+  long long cnt = 0;
+  for (int64_t j = j0; j < j1; ++j) cnt += pred(load_bits(row, j), j) ? 1 : 0;
+  long long tot;
+  const long long ex = group_excl_scan_ll(g, cnt, lscr, &tot);
+  long long found = LLONG_MAX;
+  if (ex < n && n <= ex + cnt) {
+    long long cc = ex;
+    for (int64_t j = j0; j < j1; ++j)
+      if (pred(load_bits(row, j), j) && ++cc == n) { found = j; break; }
+  }
+  return group_min_i64(g, found, lscr);
+}
+
+struct Thresholds {
+  uint32_t thr_key;
+  long long thr_n;  // kept tokens with key thr_key, first ones in id order (LLONG_MAX: all)
+  int kept;
+  float s_kept;
+  bool fallback;
+};
+
+// Exact-value window selection from sh.hist, where bin i counts the tokens whose bf16 value
+// key is top16 - i (bins [0, nb)).  Returns false when the window cannot decide (fewer than
+// k tokens in it, or less mass than the nucleus needs).  A cut inside a value keeps the
+// first tokens of that value in id order; only their number is recorded here (all of them
+// have the same probability), the id bound is found where it is needed.
+__device__ bool select_from_hist(const Group& g, RowShared& sh, const RowCtx& x, float lmax,
+                                 float s_all, uint32_t top16, int nb, Thresholds& out) {
+  const int t = threadIdx.x;
+  // consumer thread t owns bins [BPT t, BPT t + BPT), in descending value order
+  constexpr int BPT = (kWindowBins + kCons - 1) / kCons;
+  long long cnt_t = 0;
+  float e1[BPT];
+  uint32_t cn[BPT];
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    const int d = t * BPT + i;
+    cn[i] = (d < nb) ? sh.hist[d] : 0u;
+    const float v = key_value((top16 - (uint32_t)min(d, nb - 1)) << 16);
+    e1[i] = (cn[i] != 0u) ? ex2((v - lmax) * x.c) : 0.f;
+    cnt_t += cn[i];
+  }
+  long long cnt_tot;
+  const long long cnt_ex = group_excl_scan_ll(g, cnt_t, sh.lscr, &cnt_tot);
+  int dk = INT_MAX, tk = 0;
+  if (x.topk) {
+    const long long k = x.P.top_k;
+    if (t == 0) { sh.b_dk = -1; sh.b_tk = 0; }
+    g.sync();
+    if (cnt_ex < k && k <= cnt_ex + cnt_t) {
+      long long cc = cnt_ex;
+      for (int i = 0; i < BPT; ++i) {
+        if (cc + cn[i] >= k) { sh.b_dk = t * BPT + i; sh.b_tk = (int)(k - cc); break; }
+        cc += cn[i];
       }
     }
-    return;  // uniform over the cluster: no cluster barrier is pending
+    g.sync();
+    dk = sh.b_dk;
+    tk = sh.b_tk;
+    g.sync();
+    if (dk < 0) return false;  // fewer than k tokens in the window
   }
+  float m_t = 0.f;
+  float mb[BPT];
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    const int d = t * BPT + i;
+    float m = 0.f;
+    if (!x.topk || d < dk) m = (float)cn[i] * e1[i];
+    else if (d == dk) m = (float)tk * e1[i];
+    mb[i] = m;
+    m_t += m;
+  }
+  float m_tot;
+  const float m_ex = group_excl_scan(g, m_t, sh.fscr, &m_tot);
+  const float s_base = x.topk ? m_tot : s_all;
+  int my_d = INT_MAX, my_n = 0;
+  float my_before = 0.f;
+  long long my_cbefore = 0;
+  if (x.topp) {
+    const float target = (float)((double)x.P.top_p_milli / 1000.0 * (double)s_base);
+    float cum = m_ex;
+    long long cc = cnt_ex;
+    for (int i = 0; i < BPT; ++i) {
+      const int d = t * BPT + i;
+      if (x.topk && d > dk) break;
+      const float nxt = cum + mb[i];
+      if (mb[i] > 0.f && nxt >= target) {
+        const long long avail = (x.topk && d == dk) ? tk : (long long)cn[i];
+        long long n = (long long)ceil(((double)target - (double)cum) / (double)e1[i]);
+        if (n < 1) n = 1;
+        if (n > avail) n = avail;
+        my_d = d; my_n = (int)n; my_before = cum; my_cbefore = cc;
+        break;
+      }
+      cum = nxt;
+      cc += cn[i];
+    }
+  }
+  const int best = x.topp ? (int)group_min_i64(g, my_d, sh.lscr) : INT_MAX;
+  if (t == 0) sh.b_found = 0;
+  g.sync();
+  if (best != INT_MAX && my_d == best) {
+    sh.b_dp = best; sh.b_np = my_n; sh.b_mbefore = my_before; sh.b_cbefore = (int)my_cbefore;
+    sh.b_found = 1;
+  }
+  g.sync();
+  int dcut, ncut;
+  if (x.topp && sh.b_found) {
+    dcut = sh.b_dp;
+    ncut = sh.b_np;
+    const float e1c = ex2((key_value((top16 - (uint32_t)dcut) << 16) - lmax) * x.c);
+    out.s_kept = sh.b_mbefore + (float)ncut * e1c;
+    out.kept = sh.b_cbefore + ncut;
+  } else if (x.topk) {
+    dcut = dk;
+    ncut = tk;
+    out.s_kept = m_tot;
+    out.kept = (int)x.P.top_k;
+  } else {
+    g.sync();
+    return false;  // the nucleus reaches below the window
+  }
+  const uint32_t cut16 = top16 - (uint32_t)dcut;
+  const uint32_t ccut = sh.hist[dcut];
+  g.sync();
+  out.thr_key = cut16 << 16;
+  out.thr_n = ((uint32_t)ncut >= ccut) ? LLONG_MAX : ncut;
+  out.fallback = false;
+  return true;
+}
 
+// Window histogram of the tokens within dz nats below the row maximum (dz = 0: the 2048
+// values below it), from a pass over the row in L2, then the selection.
+template <typename T>
+__device__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
+                                  const RowCtx& x, int64_t V, float lmax, float s_all, float dz,
+                                  Thresholds& out) {
+  const int t = threadIdx.x;
+  const uint32_t kmax16 = order_key(__float_as_uint(lmax)) >> 16;
+  int nb = kWindowBins;
+  if ((int64_t)nb > (int64_t)kmax16 - (int64_t)(kKeyNegInf >> 16) + 1)
+    nb = (int)((int64_t)kmax16 - (int64_t)(kKeyNegInf >> 16) + 1);
+  if (dz > 0.f) {
+    const double lo = (double)lmax - (double)dz / x.scale_d;
+    if (lo > -3.0e38 && lo < (double)lmax) {
+      uint32_t klo16 = order_key(__float_as_uint((float)lo)) >> 16;
+      klo16 = klo16 > 0 ? klo16 - 1 : 0;
+      if (klo16 < kmax16 && (int64_t)(kmax16 - klo16 + 1) < nb) nb = (int)(kmax16 - klo16 + 1);
+    }
+  }
+  for (int i = t; i < kWindowBins; i += kCons) sh.hist[i] = 0u;
+  g.sync();
+  // tokens with a value >= the window's lowest value go into the histogram; only vectors
+  // whose maximum reaches the window are looked at element by element
+  const uint32_t klo16 = kmax16 - (uint32_t)(nb - 1);
+  const float wbot = key_value(klo16 << 16);
+  scan_row<T>(row, L, V, [&](const uint32_t (&b)[Elem<T>::kPerVec], long long id0, int n) {
+    float vm = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < Elem<T>::kPerVec; ++e) vm = fmaxf(vm, __uint_as_float(b[e]));
+    if (vm >= wbot) {
+      for (int e = 0; e < n; ++e)
+        if (__uint_as_float(b[e]) >= wbot) atomicAdd(&sh.hist[kmax16 - (order_key(b[e]) >> 16)], 1u);
+    }
+  });
+  g.sync();
+  return select_from_hist(g, sh, x, lmax, s_all, kmax16, nb, out);
+}
+
+// One token for the window built while the row streams.
+__device__ __forceinline__ void window_add(RowShared& sh, uint32_t bits) {
+  const uint32_t k16 = order_key(bits) >> 16;
+  if (k16 > sh.win_top16) sh.win_over = 1;
+  else atomicAdd(&sh.hist[sh.win_top16 - k16], 1u);
+}
+
+// Bits of element e of a 16-byte vector, e in [0, E) (no dynamic register indexing).
+__device__ __forceinline__ uint32_t vec_elem(const uint4& q, int e, float) {
+  return (e & 2) ? ((e & 1) ? q.w : q.z) : ((e & 1) ? q.y : q.x);
+}
+__device__ __forceinline__ uint32_t vec_elem(const uint4& q, int e, __nv_bfloat16) {
+  const uint32_t w = (e & 4) ? ((e & 2) ? q.w : q.z) : ((e & 2) ? q.y : q.x);
+  return (e & 1) ? (w & 0xFFFF0000u) : (w << 16);
+}
+
+// The window part of one ring stage: only vectors whose maximum reaches win_lo are looked
+// at, and in those only the elements that reach it (a bit mask walked with find-first-set).
+template <typename T>
+__device__ __forceinline__ void window_stage(RowShared& sh, const uint4* sv, int nv) {
+  constexpr int E = Elem<T>::kPerVec;
+  const float lo = sh.win_lo;
+  const uint32_t top16 = sh.win_top16;
+  for (int v = threadIdx.x; v < nv; v += kCons) {
+    const uint4 q = sv[v];
+    if (vec_max(q, T()) >= lo) {
+      uint32_t m = 0u;
+#pragma unroll
+      for (int e = 0; e < E; ++e) m |= (__uint_as_float(vec_elem(q, e, T())) >= lo ? 1u : 0u) << e;
+      while (m) {
+        const int e = __ffs(m) - 1;
+        m &= m - 1u;
+        const uint32_t k16 = order_key(vec_elem(q, e, T())) >> 16;
+        if (k16 > top16) sh.win_over = 1;
+        else atomicAdd(&sh.hist[top16 - k16], 1u);
+      }
+    }
+  }
+}
+
+// Generic search: bisection over the order-key space with group-wide reductions.
+template <typename T>
+__device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
+                                   const RowCtx& x, int64_t V, float lmax, uint32_t kmax_f,
+                                   Thresholds& out) {
+  auto count_ge = [&](uint32_t kk) -> long long {
+    long long cnt = 0;
+    visit_row<T>(row, L, V, [&](uint32_t bits, long long) { cnt += (order_key(bits) >= kk) ? 1 : 0; });
+    return group_sum_ll(g, cnt, sh.lscr);
+  };
+  uint32_t kk1 = 0u;
+  long long id1 = LLONG_MAX, k1count = V;
+  if (x.topk) {
+    const long long k = x.P.top_k;
+    uint32_t lo = 0u, hi = kmax_f;
+    while (lo < hi) {
+      const uint32_t mid = lo + (uint32_t)(((uint64_t)hi - lo + 1) / 2);
+      if (count_ge(mid) >= k) lo = mid; else hi = mid - 1;
+    }
+    kk1 = lo;
+    const long long above = (kk1 == 0xFFFFFFFFu) ? 0 : count_ge(kk1 + 1);
+    const long long eq = count_ge(kk1) - above;
+    const long long tt = k - above;
+    id1 = (tt < eq) ? nth_matching_id<T>(g, row, V, tt, [&](uint32_t bits, long long) { return order_key(bits) == kk1; }, sh.lscr)
+                    : LLONG_MAX;
+    k1count = k;
+  }
+  auto in_k1 = [&](uint32_t key, long long id) { return key > kk1 || (key == kk1 && id <= id1); };
+  auto mass_ge = [&](uint32_t kk) -> float {
+    float m = 0.f;
+    visit_row<T>(row, L, V, [&](uint32_t bits, long long id) {
+      const uint32_t key = order_key(bits);
+      if (key >= kk && in_k1(key, id)) m += ex2((__uint_as_float(bits) - lmax) * x.c);
+    });
+    return group_sum(g, m, sh.fscr);
+  };
+  uint32_t kcut = kk1;
+  long long idcut = id1, keptc = k1count;
+  const float s1 = mass_ge(0u);
+  float skept = s1;
+  if (x.topp) {
+    const float target = (float)((double)x.P.top_p_milli / 1000.0 * (double)s1);
+    uint32_t lo = 0u, hi = kmax_f;
+    while (lo < hi) {
+      const uint32_t mid = lo + (uint32_t)(((uint64_t)hi - lo + 1) / 2);
+      if (mass_ge(mid) >= target) lo = mid; else hi = mid - 1;
+    }
+    const uint32_t kp = lo;
+    const float above = (kp == 0xFFFFFFFFu) ? 0.f : mass_ge(kp + 1);
+    long long ca = 0, av = 0;
+    visit_row<T>(row, L, V, [&](uint32_t bits, long long id) {
+      const uint32_t key = order_key(bits);
+      if (in_k1(key, id)) { ca += (key > kp) ? 1 : 0; av += (key == kp) ? 1 : 0; }
+    });
+    const long long cnt_above = group_sum_ll(g, ca, sh.lscr);
+    const long long avail = group_sum_ll(g, av, sh.lscr);
+    const float e1 = ex2((key_value(kp) - lmax) * x.c);
+    long long n = (long long)ceil(((double)target - (double)above) / (double)e1);
+    if (n < 1) n = 1;
+    if (n > avail) n = avail;
+    kcut = kp;
+    keptc = cnt_above + n;
+    skept = above + (float)n * e1;
+    idcut = (n < avail) ? nth_matching_id<T>(g, row, V, n, [&](uint32_t bits, long long id) {
+                            const uint32_t key = order_key(bits);
+                            return key == kp && in_k1(key, id);
+                          }, sh.lscr)
+                        : (kp == kk1 ? id1 : LLONG_MAX);
+  }
+  out.thr_key = kcut;
+  out.kept = (int)keptc;
+  out.s_kept = skept;
+  out.fallback = true;
+  if (idcut == LLONG_MAX) {
+    out.thr_n = LLONG_MAX;
+  } else {  // tokens of the cut key up to idcut, in id order
+    long long cnt = 0;
+    visit_row<T>(row, L, V, [&](uint32_t bits, long long id) { cnt += (order_key(bits) == kcut && id <= idcut) ? 1 : 0; });
+    out.thr_n = group_sum_ll(g, cnt, sh.lscr);
+  }
+}
+
+// --------------------------------------------------------------------------------------
+// Consumers: finish one row after its stages were reduced.
+// --------------------------------------------------------------------------------------
+template <typename T>
+__device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, long long row_id,
+                           ThreadAcc& acc) {
+  const Group g{kCons, kConsBar};
+  const int t = threadIdx.x, w = t >> 5, l = t & 31;
   const int64_t V = A.V;
-  const T* base = reinterpret_cast<const T*>(is_target ? A.target : A.draft);
-  const T* row = base + (is_target ? row_id : row_id - R_T) * V;
+  const T* row = row_ptr<T>(A, row_id);
   const RowLayout L = row_layout(row, V);
-  const int64_t vec_lo = L.nvec * rank / C, vec_hi = L.nvec * (rank + 1) / C;
-  const bool do_head = (rank == 0), do_tail = (rank == C - 1);
+  acc_scalars_mode<T>(x.mode, acc, row, L, V, x.c);
 
-  const uint32_t tm = P.temperature_milli;
-  const bool one_hot = (tm == 0u);
-  const double scale_d = one_hot ? 0.0 : 1000.0 / (double)tm;
-  const float c = (float)(scale_d * 1.4426950408889634);  // log2(e) * 1000/T
-  const bool topk = !one_hot && want_profile && P.top_k != 0u && (int64_t)P.top_k < V;
-  const bool topp = !one_hot && want_profile && P.top_p_milli < 1000u;
-  const bool filters = topk || topp;
-  const bool need_keys = want_argmax || one_hot;
-  const bool need_sum = want_profile && !one_hot && !topk;
-  const bool need_max = want_profile && !one_hot;
-
-  // ---- pass A: one streaming read of the slice ------------------------------------
-  ThreadAcc acc;
-  acc.fm = -INFINITY; acc.s = 0.f; acc.kmax = 0u; acc.kmin = 0xFFFFFFFFu; acc.amax = LLONG_MAX; acc.bad = 0;
-  if (need_keys && need_sum)
-    stream_slice<T, true, 2>(row, L, vec_lo, vec_hi, do_head, do_tail, V, c, acc);
-  else if (need_keys && need_max)
-    stream_slice<T, true, 1>(row, L, vec_lo, vec_hi, do_head, do_tail, V, c, acc);
-  else if (need_keys)
-    stream_slice<T, true, 0>(row, L, vec_lo, vec_hi, do_head, do_tail, V, c, acc);
-  else if (need_sum)
-    stream_slice<T, false, 2>(row, L, vec_lo, vec_hi, do_head, do_tail, V, c, acc);
-  else
-    stream_slice<T, false, 1>(row, L, vec_lo, vec_hi, do_head, do_tail, V, c, acc);
-
-  // ---- block merge (fixed order) ----------------------------------------------------
-  {
-    float bfm = warp_reduce(acc.fm, [](float x, float y) { return fmax_nan(x, y); });
-    const int w = tid >> 5, l = tid & 31;
-    if (l == 0) sm.fscr[w] = bfm;
-    __syncthreads();
-    bfm = sm.fscr[0];
-    for (int i = 1; i < kWarps; ++i) bfm = fmax_nan(bfm, sm.fscr[i]);
-    float mine = (acc.s == 0.f || acc.fm == -INFINITY) ? 0.f : acc.s * ex2((acc.fm - bfm) * c);
-    if (need_sum) mine = block_sum(mine, sm.fscr); else mine = 0.f;
-    uint32_t kmx = warp_max_u32(acc.kmax), kmn = warp_min_u32(acc.kmin);
-    __syncthreads();
-    if (l == 0) { sm.lscr[w] = kmx; sm.lscr[kWarps + w] = kmn; }
-    __syncthreads();
-    kmx = 0; kmn = 0xFFFFFFFFu;
-    for (int i = 0; i < kWarps; ++i) { kmx = max(kmx, (uint32_t)sm.lscr[i]); kmn = min(kmn, (uint32_t)sm.lscr[kWarps + i]); }
-    long long am = (acc.kmax == kmx) ? acc.amax : LLONG_MAX;
-    am = block_min_i64(am, sm.lscr);
-    int bad = __syncthreads_or(acc.bad);
-    if (tid == 0) {
-      sm.part.fm = bfm; sm.part.s = mine; sm.part.kmax = kmx; sm.part.kmin = kmn;
-      sm.part.amax = am; sm.part.bad = bad;
+  // warp merge (fixed butterfly), then thread 0 merges the warps in order
+  const float wfm = warp_reduce(acc.fm, [](float a, float b) { return fmax_nan(a, b); });
+  const float mine = (acc.s == 0.f || acc.fm == -INFINITY) ? 0.f : acc.s * ex2((acc.fm - wfm) * x.c);
+  const float ws = x.need_sum ? warp_reduce(mine, [](float a, float b) { return a + b; }) : 0.f;
+  const long long wam = warp_min_i64(acc.fm == wfm ? acc.amax : LLONG_MAX);
+  if (l == 0) { sh.w_fm[w] = wfm; sh.w_s[w] = ws; sh.w_amax[w] = wam; }
+  g.sync();
+  if (t == 0) {
+    float fm = -INFINITY;
+    for (int i = 0; i < kConsWarps; ++i) fm = fmax_nan(fm, sh.w_fm[i]);
+    float s = 0.f;
+    long long am = LLONG_MAX;
+    for (int i = 0; i < kConsWarps; ++i) {
+      if (x.need_sum && sh.w_s[i] != 0.f && sh.w_fm[i] != -INFINITY) s += sh.w_s[i] * ex2((sh.w_fm[i] - fm) * x.c);
+      if (sh.w_fm[i] == fm) am = min(am, (long long)sh.w_amax[i]);
     }
+    sh.r_lmax = fm; sh.r_s = s; sh.r_amax = am;
   }
-  cluster.sync();  // S1: partials visible
+  g.sync();
+  const float lmax = sh.r_lmax;
+  const float s_all = sh.r_s;
+  const long long amax = sh.r_amax;
+  // no distribution: NaN, +inf, or no finite logit
+  int bad = (lmax != lmax || lmax == INFINITY || lmax == -INFINITY) ? 1 : 0;
+  if (x.need_sum && !(s_all < INFINITY)) bad = 1;
+  const uint32_t kmax = order_key(__float_as_uint(lmax));
+  const uint32_t kmax_f = kmax;
 
-  // ---- cluster merge in rank order (identical in every CTA) ------------------------
-  float lmax = -INFINITY, s_all = 0.f;
-  uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
-  long long amax = LLONG_MAX;
-  int bad = 0;
-  {
-    Partial pr[kMaxCluster];
-    for (unsigned r = 0; r < C; ++r) pr[r] = *cluster.map_shared_rank(&sm.part, r);
-    for (unsigned r = 0; r < C; ++r) { lmax = fmax_nan(lmax, pr[r].fm); kmax = max(kmax, pr[r].kmax); kmin = min(kmin, pr[r].kmin); bad |= pr[r].bad; }
-    for (unsigned r = 0; r < C; ++r) {
-      if (pr[r].kmax == kmax) amax = min(amax, pr[r].amax);
-      if (need_sum && pr[r].s != 0.f && pr[r].fm != -INFINITY) s_all += pr[r].s * ex2((pr[r].fm - lmax) * c);
+  Thresholds th{0u, LLONG_MAX, (int)V, s_all, false};
+  const bool filters = (x.topk || x.topp) && !bad;
+  if (filters) {
+    bool done = false;
+    if (x.window && sh.win_on) {
+      // the window built while the row streamed, plus the row's unaligned ends
+      const float lo = sh.win_lo;
+      for (int64_t j = t; j < L.head; j += kCons) {
+        const uint32_t bits = load_bits(row, j);
+        if (__uint_as_float(bits) >= lo) window_add(sh, bits);
+      }
+      for (int64_t j = L.tail0 + t; j < V; j += kCons) {
+        const uint32_t bits = load_bits(row, j);
+        if (__uint_as_float(bits) >= lo) window_add(sh, bits);
+      }
+      g.sync();
+      const bool usable = !sh.win_over && (order_key(__float_as_uint(lmax)) >> 16) <= sh.win_top16;
+      const uint32_t top16 = sh.win_top16;
+      g.sync();
+      if (usable) done = select_from_hist(g, sh, x, lmax, s_all, top16, kWindowBins, th);
     }
+    if (sizeof(T) == 2 && !done) {
+      // first window: the k-th token of top-k lies a few nats below the maximum, the top-p
+      // crossing of a broad distribution deeper
+      const float dz1 = x.topp ? 11.f : 8.f;
+      done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, dz1, th);
+      if (!done) done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, 2.f * dz1, th);
+      if (!done) done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, 0.f, th);
+    }
+    if (!done) generic_thresholds<T>(g, sh, row, L, x, V, lmax, kmax_f, th);
   }
-  if (need_keys) {
-    if (kmax >= kKeyPosInf || kmin < kKeyNegInf || kmax <= kKeyNegInf) bad = 1;
-    if (!need_max) lmax = key_value(kmax);
-  }
-  if (need_max) {
-    if (lmax != lmax || lmax == INFINITY || lmax == -INFINITY) bad = 1;
-    if (need_sum && !(s_all < INFINITY)) bad = 1;  // NaN or overflow through the sum
-  }
-  const uint32_t kmax_f = need_keys ? kmax : order_key(__float_as_uint(lmax));
-
-  // ---- filters: window histogram (bf16), else generic fallback ----------------------
-  int use_fallback = 0;
-  int kept = 0;
-  float s_kept = 1.f;
+  // the draft token of the row: kept?  (Rank among the tokens of the cut value when the cut
+  // falls inside that value; rare, so it is counted here over the ids before it.)
   uint32_t thr_key = 0u;
-  long long thr_id = LLONG_MAX;
-  bool need_final_fallback = false;
-  Decision dec{};
-  const bool do_filters = filters && !bad;
-  if (do_filters) {
-    const bool is_bf16 = (sizeof(T) == 2);
-    const uint32_t kmax16 = kmax_f >> 16;
-    int nb = kWindowBins;
-    if (is_bf16) {
-      if ((int64_t)nb > (int64_t)kmax16 - (int64_t)(kKeyNegInf >> 16) + 1)
-        nb = (int)((int64_t)kmax16 - (int64_t)(kKeyNegInf >> 16) + 1);
-      if (topp && !topk && s_all > 0.f) {
-        // Tokens more than R below the max (z units) hold < 1% of the (1-P) mass left
-        // outside the nucleus, so the crossing lies above them.
-        double R = log((double)V / (0.01 * (1.0 - P.top_p_milli / 1000.0) * (double)s_all));
-        double lo = (double)lmax - R / scale_d;
-        if (lo > -3.0e38 && lo < (double)lmax) {
-          uint32_t klo16 = order_key(__float_as_uint((float)lo)) >> 16;
-          klo16 = klo16 > 0 ? klo16 - 1 : 0;
-          if (klo16 < kmax16 && (int64_t)(kmax16 - klo16 + 1) < nb) nb = (int)(kmax16 - klo16 + 1);
-        }
-      }
-      for (int i = tid; i < kWindowBins; i += kThreads) sm.hist[i] = 0u;
-      __syncthreads();
-      visit_slice<T>(row, L, vec_lo, vec_hi, do_head, do_tail, V, [&](uint32_t bits, long long) {
-        uint32_t d = kmax16 - (order_key(bits) >> 16);
-        if (d < (uint32_t)nb) atomicAdd(&sm.hist[d], 1u);
-      });
-      __syncthreads();
-    }
-    cluster.sync();  // S2: histograms visible
-    if (rank == 0) {
-      if (tid == 0) { sm.dec = Decision{}; sm.dec.use_fallback = is_bf16 ? 0 : 1; }
-      __syncthreads();
-      if (is_bf16) {
-        // sum the cluster's histograms into rank 0's (rank order; integer: exact)
-        for (unsigned r = 1; r < C; ++r) {
-          const uint32_t* rh = cluster.map_shared_rank(sm.hist, r);
-          for (int i = tid; i < nb; i += kThreads) sm.hist[i] += rh[i];
-        }
-        __syncthreads();
-        // thread t owns bins [8t, 8t+8), in descending value order
-        constexpr int BPT = kWindowBins / kThreads;
-        long long cnt_t = 0;
-        float e1[BPT];
-        uint32_t cn[BPT];
-#pragma unroll
-        for (int i = 0; i < BPT; ++i) {
-          int d = tid * BPT + i;
-          cn[i] = (d < nb) ? sm.hist[d] : 0u;
-          float v = key_value((kmax16 - (uint32_t)min(d, nb - 1)) << 16);
-          e1[i] = (d < nb) ? ex2((v - lmax) * c) : 0.f;
-          cnt_t += cn[i];
-        }
-        long long cnt_tot;
-        long long cnt_ex = block_exclusive_scan_ll(cnt_t, sm.lscr, &cnt_tot);
-        // top-k: the bin of the k-th token and how many of its tokens are kept
-        int dk = INT_MAX, tk = 0;
-        if (topk) {
-          const long long k = P.top_k;
-          if (tid == 0) { sm.b_dk = -1; sm.b_tk = 0; }
-          __syncthreads();
-          if (cnt_ex < k && k <= cnt_ex + cnt_t) {
-            long long cc = cnt_ex;
-            for (int i = 0; i < BPT; ++i) {
-              if (cc + cn[i] >= k) { sm.b_dk = tid * BPT + i; sm.b_tk = (int)(k - cc); break; }
-              cc += cn[i];
-            }
-          }
-          __syncthreads();
-          dk = sm.b_dk; tk = sm.b_tk;
-        }
-        if (topk && dk < 0) {
-          if (tid == 0) sm.dec.use_fallback = 1;  // fewer than k tokens in the window
+  long long thr_n = LLONG_MAX;
+  if (x.one_hot) { thr_key = kmax; thr_n = 1; }
+  else if (filters) { thr_key = th.thr_key; thr_n = th.thr_n; }
+  int32_t xt = -1;
+  uint32_t xb = 0u;
+  bool kept_x = false;
+  if (x.has_x && !bad) {
+    xt = A.tokens[x.tok_idx];
+    if (xt >= 0 && (int64_t)xt < V) {
+      xb = load_bits(row, xt);
+      const uint32_t xk = order_key(xb);
+      if (x.one_hot) {
+        kept_x = (xt == amax);
+      } else if (xk > thr_key) {
+        kept_x = true;
+      } else if (xk == thr_key) {
+        if (thr_n == LLONG_MAX) {
+          kept_x = true;
         } else {
-          // masses of the kept top-k bins (bins past dk hold nothing, bin dk holds tk)
-          float m_t = 0.f;
-          float mb[BPT];
-#pragma unroll
-          for (int i = 0; i < BPT; ++i) {
-            int d = tid * BPT + i;
-            float m = 0.f;
-            if (!topk || d < dk) m = (float)cn[i] * e1[i];
-            else if (d == dk) m = (float)tk * e1[i];
-            mb[i] = m;
-            m_t += m;
-          }
-          float m_tot;
-          float m_ex = block_exclusive_scan(m_t, sm.fscr, &m_tot);
-          const float s_base = topk ? m_tot : s_all;
-          int my_d = INT_MAX, my_n = 0;
-          float my_before = 0.f;
-          long long my_cbefore = 0;
-          if (topp) {
-            // the first bin whose cumulative mass reaches P * S, and how many of its
-            // (equal-mass) tokens are needed
-            const float target = (float)((double)P.top_p_milli / 1000.0 * (double)s_base);
-            float cum = m_ex;
-            long long cc = cnt_ex;
-            for (int i = 0; i < BPT; ++i) {
-              int d = tid * BPT + i;
-              if (topk && d > dk) break;
-              float nxt = cum + mb[i];
-              if (mb[i] > 0.f && nxt >= target) {
-                long long avail = (topk && d == dk) ? tk : (long long)cn[i];
-                double need = ceil(((double)target - (double)cum) / (double)e1[i]);
-                long long n = (long long)need;
-                if (n < 1) n = 1;
-                if (n > avail) n = avail;
-                my_d = d; my_n = (int)n; my_before = cum; my_cbefore = cc;
-                break;
-              }
-              cum = nxt;
-              cc += cn[i];
-            }
-          }
-          int best = topp ? (int)block_min_i64(my_d, sm.lscr) : INT_MAX;
-          if (tid == 0) sm.b_found = 0;
-          __syncthreads();
-          if (best != INT_MAX && my_d == best) {
-            sm.b_dp = best; sm.b_np = my_n; sm.b_massbefore_p = my_before;
-            sm.b_countbefore_p = (int)my_cbefore; sm.b_found = 1;
-          }
-          __syncthreads();
-          if (tid == 0) {
-            Decision d0{};
-            if (topp && sm.b_found) {
-              const int dcut = sm.b_dp, ncut = sm.b_np;
-              const float e1c = ex2((key_value((kmax16 - (uint32_t)dcut) << 16) - lmax) * c);
-              d0.s_kept = sm.b_massbefore_p + (float)ncut * e1c;
-              d0.kept = sm.b_countbefore_p + ncut;
-              d0.thr_key = (kmax16 - (uint32_t)dcut) << 16;
-              d0.need_tie = (ncut < (int)sm.hist[dcut]) ? 1 : 0;
-              d0.tie_key16 = kmax16 - (uint32_t)dcut;
-              d0.tie_n = ncut;
-            } else if (topk) {
-              // top-k alone, or a nucleus that covers the whole top-k set
-              d0.s_kept = m_tot;
-              d0.kept = (int)P.top_k;
-              d0.thr_key = (kmax16 - (uint32_t)dk) << 16;
-              d0.need_tie = (tk < (int)sm.hist[dk]) ? 1 : 0;
-              d0.tie_key16 = kmax16 - (uint32_t)dk;
-              d0.tie_n = tk;
-            } else {
-              d0.use_fallback = 1;  // the nucleus reaches below the window
-            }
-            sm.dec = d0;
-          }
+          long long before = 0;
+          for (int64_t j = t; j < xt; j += kCons) before += (order_key(load_bits(row, j)) == thr_key) ? 1 : 0;
+          kept_x = group_sum_ll(g, before, sh.lscr) < thr_n;
         }
       }
-    }
-    cluster.sync();  // S3: decision visible
-    dec = *cluster.map_shared_rank(&sm.dec, 0);
-    if (!dec.use_fallback && dec.need_tie) {
-      // tie pass: ids with the cut value in this CTA's slice
-      if (tid == 0) sm.tie_count = 0;
-      __syncthreads();
-      const uint32_t tk16 = dec.tie_key16;
-      visit_slice<T>(row, L, vec_lo, vec_hi, do_head, do_tail, V, [&](uint32_t bits, long long id) {
-        if ((order_key(bits) >> 16) == tk16) {
-          int slot = atomicAdd(&sm.tie_count, 1);
-          if (slot < kTieListCap) sm.tie_ids[slot] = (int)id;
-        }
-      });
-      __syncthreads();
-      cluster.sync();  // S4: tie lists visible
-      if (rank == 0) {
-        // find the CTA (id order = rank order) holding the n-th tied id
-        int before = 0, owner = -1, overflow = 0, cnt_owner = 0;
-        for (unsigned r = 0; r < C; ++r) {
-          int cr = *cluster.map_shared_rank(&sm.tie_count, r);
-          if (owner < 0 && before + cr >= dec.tie_n) { owner = (int)r; cnt_owner = cr; }
-          else if (owner < 0) before += cr;
-        }
-        if (owner < 0 || cnt_owner > kTieListCap) overflow = 1;
-        if (tid == 0) sm.b_tie_id = -1;
-        __syncthreads();
-        if (!overflow) {
-          const int* ids = cluster.map_shared_rank(sm.tie_ids, (unsigned)owner);
-          const int want = dec.tie_n - before;  // 1-based within the owner's list
-          for (int i = tid; i < cnt_owner; i += kThreads) {
-            int my = ids[i], rnk = 0;
-            for (int j = 0; j < cnt_owner; ++j) rnk += (ids[j] < my) ? 1 : 0;
-            if (rnk == want - 1) sm.b_tie_id = my;
-          }
-        }
-        __syncthreads();
-        thr_id = (sm.b_tie_id >= 0) ? (long long)sm.b_tie_id : LLONG_MAX;
-        if (overflow || sm.b_tie_id < 0) need_final_fallback = true;  // generic id search
-      }
-    }
-    if (!dec.use_fallback) {
-      thr_key = dec.thr_key;
-      kept = dec.kept;
-      s_kept = dec.s_kept;
-      if (!dec.need_tie) thr_id = LLONG_MAX;
     } else {
-      use_fallback = 1;
+      xt = -2;  // out of range: reported through the session status
     }
   }
-  cluster.sync();  // final: no CTA reads another's shared memory after this
-  if (rank != 0) return;
-
-  // ---- rank 0 alone from here ---------------------------------------------------------
-  WholeRow<T> R{row, L, V};
-  uint32_t flags = 0;
-  if (bad) flags |= SDCP_ROW_INVALID;
-
-  if (!bad && do_filters && need_final_fallback && !use_fallback) {
-    // tie list overflowed: find the tie_n-th id with the cut value over the whole row
-    const uint32_t tk16 = dec.tie_key16;
-    thr_id = nth_matching_id<T>(R, dec.tie_n, [&](uint32_t bits, long long) {
-      return (order_key(bits) >> 16) == tk16;
-    }, sm.lscr);
-  }
-  if (!bad && do_filters && use_fallback) {
-    flags |= SDCP_ROW_FALLBACK;
-    // Generic search: bisection over the order-key space with block-wide reductions.
-    auto count_ge = [&](uint32_t kk) -> long long {
-      long long cnt = 0;
-      R.visit([&](uint32_t bits, long long) { cnt += (order_key(bits) >= kk) ? 1 : 0; });
-      return block_sum_ll(cnt, sm.lscr);
-    };
-    uint32_t kk1 = 0u;
-    long long id1 = LLONG_MAX, k1count = V;
-    if (topk) {
-      const long long k = P.top_k;
-      uint32_t lo = 0u, hi = kmax_f;  // count_ge(lo) >= k, answer in [lo, hi]
-      while (lo < hi) {
-        uint32_t mid = lo + (uint32_t)(((uint64_t)hi - lo + 1) / 2);
-        if (count_ge(mid) >= k) lo = mid; else hi = mid - 1;
-      }
-      kk1 = lo;
-      long long above = (kk1 == 0xFFFFFFFFu) ? 0 : count_ge(kk1 + 1);
-      long long eq = count_ge(kk1) - above;
-      long long t = k - above;
-      id1 = (t < eq) ? nth_matching_id<T>(R, t, [&](uint32_t bits, long long) { return order_key(bits) == kk1; }, sm.lscr)
-                     : LLONG_MAX;
-      k1count = k;
-    }
-    auto in_k1 = [&](uint32_t key, long long id) { return key > kk1 || (key == kk1 && id <= id1); };
-    auto mass_ge = [&](uint32_t kk) -> float {
-      float m = 0.f;
-      R.visit([&](uint32_t bits, long long id) {
-        uint32_t key = order_key(bits);
-        if (key >= kk && in_k1(key, id)) m += ex2((__uint_as_float(bits) - lmax) * c);
-      });
-      return block_sum(m, sm.fscr);
-    };
-    uint32_t kcut = kk1;
-    long long idcut = id1, keptc = k1count;
-    float s1 = mass_ge(0u);
-    float skept = s1;
-    if (topp) {
-      const float target = (float)((double)P.top_p_milli / 1000.0 * (double)s1);
-      uint32_t lo = 0u, hi = kmax_f;  // mass_ge(lo) >= target (s1 >= target)
-      while (lo < hi) {
-        uint32_t mid = lo + (uint32_t)(((uint64_t)hi - lo + 1) / 2);
-        if (mass_ge(mid) >= target) lo = mid; else hi = mid - 1;
-      }
-      const uint32_t kp = lo;
-      const float above = (kp == 0xFFFFFFFFu) ? 0.f : mass_ge(kp + 1);
-      long long cnt_above = 0, avail = 0;
-      {
-        long long ca = 0, av = 0;
-        R.visit([&](uint32_t bits, long long id) {
-          uint32_t key = order_key(bits);
-          if (in_k1(key, id)) { ca += (key > kp) ? 1 : 0; av += (key == kp) ? 1 : 0; }
-        });
-        cnt_above = block_sum_ll(ca, sm.lscr);
-        avail = block_sum_ll(av, sm.lscr);
-      }
-      const float e1 = ex2((key_value(kp) - lmax) * c);
-      long long n = (long long)ceil(((double)target - (double)above) / (double)e1);
-      if (n < 1) n = 1;
-      if (n > avail) n = avail;
-      kcut = kp;
-      keptc = cnt_above + n;
-      skept = above + (float)n * e1;
-      idcut = (n < avail) ? nth_matching_id<T>(R, n, [&](uint32_t bits, long long id) {
-                              uint32_t key = order_key(bits);
-                              return key == kp && in_k1(key, id);
-                            }, sm.lscr)
-                          : (kp == kk1 ? id1 : LLONG_MAX);
-    } else {
-      skept = s1;
-    }
-    thr_key = kcut;
-    thr_id = idcut;
-    kept = (int)keptc;
-    s_kept = skept;
-  }
-
-  if (tid != 0) return;
+  g.sync();  // shared scratch of this row is free again after this point
+  if (t != 0) return;
+  uint32_t flags = bad ? SDCP_ROW_INVALID : 0u;
+  if (filters && th.fallback) flags |= SDCP_ROW_FALLBACK;
   RowStat st;
   st.lmax = lmax;
   st.argmax = (amax == LLONG_MAX) ? -1 : (int32_t)amax;
-  if (one_hot) {
-    st.s = 1.f;
-    st.thr_key = kmax;
-    st.thr_id = st.argmax;
-    st.kept = 1;
-  } else if (do_filters) {
-    st.s = s_kept;
-    st.thr_key = thr_key;
-    st.thr_id = (thr_id == LLONG_MAX) ? INT_MAX : (int32_t)thr_id;
-    st.kept = kept;
+  st.thr_key = thr_key;
+  st.thr_n = (thr_n == LLONG_MAX) ? INT_MAX : (int32_t)thr_n;
+  if (x.one_hot) {
+    st.s = 1.f; st.kept = 1;
+  } else if (filters) {
+    st.s = th.s_kept; st.kept = th.kept;
   } else {
-    st.s = s_all;
-    st.thr_key = 0u;
-    st.thr_id = INT_MAX;
-    st.kept = (int32_t)V;
+    st.s = s_all; st.kept = (int32_t)V;
   }
   st.dlx = __int_as_float(0x7FC00000);
-  if (has_x && !bad) {
-    const int32_t x = A.tokens[tok_idx];
-    if (x >= 0 && (int64_t)x < V) {
-      flags |= kRowHasX;
-      const uint32_t xb = load_bits(row, x);
-      const float lx = __uint_as_float(xb);
-      const uint32_t xk = order_key(xb);
-      const bool kept_x = one_hot ? (x == st.argmax)
-                                  : (xk > st.thr_key || (xk == st.thr_key && x <= st.thr_id));
-      st.dlx = lx - lmax;
-      if (kept_x && lx != -INFINITY) flags |= SDCP_ROW_X_KEPT;
-    }
+  if (xt >= 0) {
+    flags |= kRowHasX;
+    const float lx = __uint_as_float(xb);
+    st.dlx = lx - lmax;
+    if (kept_x && lx != -INFINITY) flags |= SDCP_ROW_X_KEPT;
   }
   st.flags = flags;
-  *out = st;
+  A.stats[row_id] = st;
   if (A.pub) {
     sdcp_row_stat q;
     q.lmax = st.lmax;
@@ -695,41 +760,187 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(RowArgs A) {
     q.argmax = st.argmax;
     q.kept = st.kept;
     q.thr_key = st.thr_key;
-    q.thr_id = st.thr_id;
+    q.thr_n = st.thr_n;
     q.flags = flags & ~kRowHasX;
     if (!(flags & kRowHasX)) q.lp_x = __int_as_float(0x7FC00000);
     else if (!(flags & SDCP_ROW_X_KEPT)) q.lp_x = -INFINITY;
-    else if (one_hot) q.lp_x = 0.f;
-    else q.lp_x = (float)((double)st.dlx * scale_d - log((double)st.s));
+    else if (x.one_hot) q.lp_x = 0.f;
+    else q.lp_x = (float)((double)st.dlx * x.scale_d - log((double)st.s));
     A.pub[row_id] = q;
   }
+}
+
+// --------------------------------------------------------------------------------------
+// The persistent row kernel.
+// --------------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(RowArgs A) {
+  extern __shared__ __align__(128) unsigned char ring[];  // kStages * kChunk bytes
+  __shared__ RowShared sh;
+  const int t = threadIdx.x, w = t >> 5, l = t & 31;
+  const long long nrows = A.total + A.B + A.total;
+
+  pdl_launch_dependents();  // the session kernel may start its prologue now
+  if (t == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&sh.full[s], 1); mbar_init(&sh.empty[s], kConsWarps); }
+    sh.abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (w == kProducerWarp) {
+    // ---------------- producer: stream the CTA's rows into the ring ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    // session of a row (warp-cooperative search); the next row's is looked up while the
+    // current row streams, so its latency is hidden behind the copies in flight
+    auto session_of = [&](long long r) -> int {
+      const bool is_target = r < A.total + A.B;
+      return find_session(A.m_offsets, A.B, is_target ? r : r - (A.total + A.B), is_target);
+    };
+    long long r = blockIdx.x;
+    int b = (r < nrows) ? session_of(r) : 0;
+    for (; r < nrows && ok; r += gridDim.x) {
+      const RowCtx x = row_ctx(A, r, b, sizeof(T) == 2);
+      const long long rn = r + gridDim.x;
+      int bn = 0;
+      if (x.skip) {
+        if (l == 0) write_skipped(A, r);
+        b = (rn < nrows) ? session_of(rn) : 0;
+        continue;
+      }
+      const T* row = row_ptr<T>(A, r);
+      const RowLayout L = row_layout(row, A.V);
+      const long long vbytes = L.nvec * 16;
+      const int nch = (int)max(1ll, (vbytes + kChunk - 1) / kChunk);
+      const char* src = reinterpret_cast<const char*>(row + L.head);
+      for (int c = 0; c < nch && ok; ++c) {
+        if (l == 0) {
+          if (!mbar_wait(&sh.empty[stage], phase ^ 1u, kWaitPolls) || sh.abort) {
+            ok = false;
+          } else {
+            const long long off = (long long)c * kChunk;
+            const uint32_t bytes = (uint32_t)max(0ll, min((long long)kChunk, vbytes - off));
+            if (c == 0) { sh.plan[stage].row_id = r; sh.plan[stage].b = b; sh.plan[stage].nchunks = nch; }
+            mbar_arrive_expect_tx(&sh.full[stage], bytes);
+            if (bytes > 0) bulk_copy_g2s(ring + (size_t)stage * kChunk, src + off, bytes, &sh.full[stage]);
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (c == 0 && rn < nrows) bn = session_of(rn);  // overlaps the copies in flight
+      }
+      b = bn;
+    }
+    if (l == 0) {
+      if (ok && mbar_wait(&sh.empty[stage], phase ^ 1u, kWaitPolls) && !sh.abort) {
+        sh.plan[stage].row_id = -1;
+        mbar_arrive_expect_tx(&sh.full[stage], 0);
+      } else {
+        sh.abort = 1;
+        atomicOr(A.error, 1u);
+        // let copies already issued land before the CTA can exit (bounded)
+        for (int s = 0; s < kStages; ++s) {
+          (void)mbar_wait(&sh.full[s], 0, 1 << 12);
+          (void)mbar_wait(&sh.full[s], 1, 1 << 12);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const Group g{kCons, kConsBar};
+  int stage = 0;
+  uint32_t phase = 0;
+  ThreadAcc acc;
+  acc.reset();
+  while (true) {
+    if (!mbar_wait(&sh.full[stage], phase, kWaitPolls)) sh.abort = 1;
+    g.sync();
+    if (sh.abort) break;
+    const RowPlan plan = sh.plan[stage];
+    if (plan.row_id < 0) break;
+    const RowCtx x = row_ctx(A, plan.row_id, plan.b, sizeof(T) == 2);
+    const T* row = row_ptr<T>(A, plan.row_id);
+    const RowLayout L = row_layout(row, A.V);
+    if (x.window) {  // fresh window for this row (ordered before use by the barrier below)
+      for (int i = t; i < kWindowBins; i += kCons) sh.hist[i] = 0u;
+      if (t == 0) sh.win_over = 0;
+    }
+    bool fail = false;
+    for (int c = 0; c < plan.nchunks; ++c) {
+      if (c > 0 && !mbar_wait(&sh.full[stage], phase, kWaitPolls)) { fail = true; break; }
+      const long long off = (long long)c * kChunk;
+      const int nv = (int)(max(0ll, min((long long)kChunk, L.nvec * 16 - off)) / 16);
+      const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)stage * kChunk);
+      const long long id0 = L.head + (off / 16) * Elem<T>::kPerVec;
+      acc_stage_mode<T>(x.mode, acc, sv, nv, id0, x.c);
+      if (x.window) {
+        if (c == 0) {
+          // anchor: the maximum of the first stage; the window keeps every token within
+          // dz nats of it, and room for values up to 2047 bf16 steps above its bottom
+          const float wm = warp_reduce(acc.fm, [](float a, float b) { return fmax_nan(a, b); });
+          if (l == 0) sh.w_fm[w] = wm;
+          g.sync();
+          if (t == 0) {
+            float m0 = -INFINITY;
+            for (int i = 0; i < kConsWarps; ++i) m0 = fmax_nan(m0, sh.w_fm[i]);
+            const float dz = x.topp ? 11.f : 8.f;
+            const double lo = (double)m0 - (double)dz / x.scale_d;
+            sh.win_on = (m0 == m0 && m0 > -INFINITY && m0 < INFINITY && lo > -3.0e38) ? 1 : 0;
+            if (sh.win_on) {
+              uint32_t lo16 = order_key(__float_as_uint((float)lo)) >> 16;
+              lo16 = lo16 > (kKeyNegInf >> 16) ? lo16 - 1 : (kKeyNegInf >> 16);
+              sh.win_lo = key_value(lo16 << 16);
+              sh.win_top16 = min(lo16 + (uint32_t)(kWindowBins - 1), 0xFF7Fu);
+            }
+          }
+          g.sync();
+        }
+        if (sh.win_on) window_stage<T>(sh, sv, nv);
+      }
+      __syncwarp();
+      if (l == 0) mbar_arrive(&sh.empty[stage]);
+      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+    }
+    if (fail) sh.abort = 1;
+    g.sync();
+    if (sh.abort) break;
+    finish_row<T>(A, sh, x, plan.row_id, acc);
+    acc.reset();
+  }
+  if (t == 0 && sh.abort) atomicOr(A.error, 1u);
 }
 
 template __global__ void row_stats_kernel<float>(RowArgs);
 template __global__ void row_stats_kernel<__nv_bfloat16>(RowArgs);
 
-// Host-side launcher.
-int launch_row_stats(const RowArgs& a, int dtype, int cluster, cudaStream_t stream) {
-  int64_t rows = a.total + a.B + a.total;
+int launch_row_stats(const RowArgs& a, int dtype, cudaStream_t stream) {
+  const long long rows = a.total + a.B + a.total;
   if (rows <= 0) return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(rows * cluster), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return (int)cudaErrorInvalidDevice;
+  const size_t ring_bytes = (size_t)kStages * kChunk;
+  const void* fn = (dtype == SDCP_BF16) ? (const void*)row_stats_kernel<__nv_bfloat16>
+                                        : (const void*)row_stats_kernel<float>;
+  // all of the unified L1/shared storage as shared memory, so two CTAs fit on an SM
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring_bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return (int)e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRowThreads, ring_bytes);
+  if (e != cudaSuccess) return (int)e;
+  if (per_sm < 1) per_sm = 1;
+  const long long grid = min(rows, (long long)sms * min(per_sm, kRowCtasPerSm));
   if (dtype == SDCP_BF16)
-    e = cudaLaunchKernelEx(&cfg, row_stats_kernel<__nv_bfloat16>, a);
+    row_stats_kernel<__nv_bfloat16><<<(unsigned)grid, kRowThreads, ring_bytes, stream>>>(a);
   else
-    e = cudaLaunchKernelEx(&cfg, row_stats_kernel<float>, a);
-  if (e == cudaSuccess) e = cudaGetLastError();
+    row_stats_kernel<float><<<(unsigned)grid, kRowThreads, ring_bytes, stream>>>(a);
+  e = cudaGetLastError();
   return e == cudaSuccess ? 0 : (int)e;
 }
 

@@ -26,7 +26,7 @@ PARAMS_DTYPE = np.dtype([("rule_id", "<u4"), ("temperature_milli", "<u4"), ("top
                          ("top_p_milli", "<u4"), ("seed", "<u8"), ("round", "<u4"),
                          ("session_tag", "<u4")])
 ROW_STAT_DTYPE = np.dtype([("lmax", "<f4"), ("log_s", "<f4"), ("lp_x", "<f4"), ("argmax", "<i4"),
-                           ("kept", "<i4"), ("thr_key", "<u4"), ("thr_id", "<i4"), ("flags", "<u4")])
+                           ("kept", "<i4"), ("thr_key", "<u4"), ("thr_n", "<i4"), ("flags", "<u4")])
 
 
 class SdcpError(RuntimeError):
