@@ -1,5 +1,7 @@
 // sdcp_abi.cu - the C ABI of libsdcp (declared in include/sdcp.h): argument checks on
-// the host, workspace layout, cluster sizes, and the two launches on the caller's stream.
+// the host, the workspace layout, and the launches on the caller's stream: a clear of the
+// workspace header, the row kernel, then the session kernel (a programmatic dependent of
+// the row kernel in sdcp_verify_batch).
 #include <climits>
 
 #include "sdcp_device.cuh"
@@ -11,26 +13,13 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// CTAs per session cluster for the draw: enough sessions x CTAs to cover the SMs when the
-// batch is small, never slices under 16 KB of one row; 1..8.
-int session_cluster(int64_t V, int dtype, int32_t B) {
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 148;
-  const int64_t bytes = V * (dtype == SDCP_BF16 ? 2 : 4);
-  int64_t c = (sms + (int64_t)B - 1) / (B > 0 ? B : 1);
-  const int64_t by_size = (bytes + 16383) / 16384;
-  if (c > by_size) c = by_size;
-  return (int)(c < 1 ? 1 : (c > kMaxCluster ? kMaxCluster : c));
-}
-
 int check_common(const void* target, int dtype, int64_t V, int32_t B, const int32_t* m_offsets,
                  int64_t total, const int32_t* tokens, const sdcp_session_params* params,
                  const void* draft) {
   if (B < 0 || total < 0 || V < 1) return SDCP_E_INVALID;
   if (dtype != SDCP_F32 && dtype != SDCP_BF16) return SDCP_E_INVALID;
   if (V > SDCP_MAX_VOCAB) return SDCP_E_TOO_LARGE;
-  if (total + B + total > (int64_t)INT32_MAX / kMaxCluster) return SDCP_E_TOO_LARGE;
+  if (total + B + total > (int64_t)INT32_MAX / 2) return SDCP_E_TOO_LARGE;
   if (B == 0) return SDCP_OK;
   if (!target || !m_offsets || !params || (total > 0 && !tokens)) return SDCP_E_INVALID;
   const size_t esz = dtype == SDCP_BF16 ? 2 : 4;
@@ -57,6 +46,24 @@ int check_workspace(void* workspace, size_t workspace_bytes, int64_t V, int32_t 
       workspace_bytes < sdcp_workspace_bytes(V, B, total))
     return SDCP_E_WORKSPACE;
   return SDCP_OK;
+}
+
+// The session inputs and outputs, with the workspace's statistics and error word.
+SessIO make_io(const void* target, const void* draft, int64_t V, int32_t B, const int32_t* m_offsets,
+               int64_t total, const int32_t* tokens, const sdcp_session_params* params,
+               int32_t* accepted, int32_t* n_out, int32_t* out_tokens, int32_t* status, void* ws) {
+  char* w = static_cast<char*>(ws);
+  return SessIO{target, draft, V, B, m_offsets, total, tokens, params,
+                reinterpret_cast<const RowStat*>(w + kWsHeader),
+                accepted, n_out, out_tokens, status, reinterpret_cast<const uint32_t*>(w)};
+}
+
+// Clears the header, then launches the row kernel.
+int launch_rows(const SessIO& io, void* ws, sdcp_row_stat* pub, int stats_mode, int dtype, cudaStream_t s) {
+  char* w = static_cast<char*>(ws);
+  if (cudaMemsetAsync(w, 0, kWsHeader, s) != cudaSuccess) return SDCP_E_LAUNCH;
+  RowArgs ra{io, const_cast<RowStat*>(io.stats), pub, stats_mode, reinterpret_cast<WsHeader*>(w)};
+  return launch_row_stats(ra, dtype, s) != 0 ? SDCP_E_LAUNCH : SDCP_OK;
 }
 }  // namespace
 }  // namespace sdcp
@@ -92,13 +99,9 @@ int sdcp_verify_rows(const void* target_logits, const void* draft_logits, int dt
   if (B == 0) return SDCP_OK;
   rc = check_workspace(workspace, workspace_bytes, V, B, total_drafts);
   if (rc != SDCP_OK) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t* err = reinterpret_cast<uint32_t*>(workspace);
-  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return SDCP_E_LAUNCH;
-  RowArgs ra{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
-             reinterpret_cast<RowStat*>(static_cast<char*>(workspace) + kWsHeader), nullptr, 0, err};
-  if (launch_row_stats(ra, dtype, s) != 0) return SDCP_E_LAUNCH;
-  return SDCP_OK;
+  const SessIO io = make_io(target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens,
+                            params, nullptr, nullptr, nullptr, nullptr, workspace);
+  return launch_rows(io, workspace, nullptr, 0, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 static int verify_sessions(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
@@ -113,12 +116,9 @@ static int verify_sessions(const void* target_logits, const void* draft_logits, 
   if (!accepted || !n_out || !out_tokens || !status) return SDCP_E_INVALID;
   rc = check_workspace(workspace, workspace_bytes, V, B, total_drafts);
   if (rc != SDCP_OK) return rc;
-  const char* ws = static_cast<const char*>(workspace);
-  SessArgs sa{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
-              reinterpret_cast<const RowStat*>(ws + kWsHeader), accepted, n_out, out_tokens, status,
-              reinterpret_cast<const uint32_t*>(ws)};
-  if (launch_sessions(sa, dtype, session_cluster(V, dtype, B), pdl, reinterpret_cast<cudaStream_t>(stream)) != 0)
-    return SDCP_E_LAUNCH;
+  const SessIO io = make_io(target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens,
+                            params, accepted, n_out, out_tokens, status, workspace);
+  if (launch_sessions(io, dtype, pdl, reinterpret_cast<cudaStream_t>(stream)) != 0) return SDCP_E_LAUNCH;
   return SDCP_OK;
 }
 
@@ -164,13 +164,9 @@ int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtyp
   if (total_drafts > 0 && !draft_logits) return SDCP_E_INVALID;
   rc = check_workspace(workspace, workspace_bytes, V, B, total_drafts);
   if (rc != SDCP_OK) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t* err = reinterpret_cast<uint32_t*>(workspace);
-  if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return SDCP_E_LAUNCH;
-  RowArgs ra{target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
-             reinterpret_cast<RowStat*>(static_cast<char*>(workspace) + kWsHeader), stats_out, 1, err};
-  if (launch_row_stats(ra, dtype, s) != 0) return SDCP_E_LAUNCH;
-  return SDCP_OK;
+  const SessIO io = make_io(target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens,
+                            params, nullptr, nullptr, nullptr, nullptr, workspace);
+  return launch_rows(io, workspace, stats_out, 1, dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -13,12 +13,10 @@ namespace sdcp {
 
 namespace cg = cooperative_groups;
 
-constexpr int kThreads = 256;          // threads per CTA of both kernels
+constexpr int kThreads = 256;          // threads of a group that runs a session completion
 constexpr int kWarps = kThreads / 32;
 constexpr int kWindowBins = 2048;      // exact bf16 keys below the row maximum
-constexpr int kTieListCap = 256;       // ids with the cut key, per CTA
-constexpr int kMaxCluster = 8;
-constexpr int kEpt = 8;                // elements per thread per tile (draw kernel)
+constexpr int kEpt = 8;                // ids per lane piece of the draw passes
 
 // Internal per-row record written by the row kernel (workspace), 32 bytes.
 struct RowStat {
@@ -35,24 +33,17 @@ constexpr uint32_t kRowHasX = 16u;     // the row carries a draft token that is 
 
 static_assert(sizeof(RowStat) == 32, "RowStat layout");
 
-// Arguments of the row kernel (phase 1).
-struct RowArgs {
-  const void* target;
-  const void* draft;
-  int64_t V;
-  int32_t B;
-  const int32_t* m_offsets;
-  int64_t total;              // sum of M (host value)
-  const int32_t* tokens;
-  const sdcp_session_params* params;
-  RowStat* stats;             // [total + B + total]: target rows, then draft rows
-  sdcp_row_stat* pub;         // optional public copy (statistics mode)
-  int stats_mode;             // 1: every row gets the full statistics
-  uint32_t* error;            // workspace word: non-zero if a bounded wait gave up
+// Workspace: a 256-byte header (cleared before every call), then one RowStat per scored
+// row (target rows, then draft rows).
+struct WsHeader {
+  uint32_t error;                // non-zero: a bounded wait gave up
+  uint32_t pad;
+  unsigned long long next_slot;  // next row of the dynamic schedule
 };
+constexpr size_t kWsHeader = 256;
 
-// Arguments of the session kernel (phase 2).
-struct SessArgs {
+// Everything a session completion reads and writes.
+struct SessIO {
   const void* target;
   const void* draft;
   int64_t V;
@@ -66,14 +57,20 @@ struct SessArgs {
   int32_t* n_out;
   int32_t* out_tokens;
   int32_t* status;
-  const uint32_t* error;      // the row kernel's error word
+  const uint32_t* error;  // non-zero: a bounded wait of the call gave up
 };
 
-// Workspace: [0, 256) error word, then one RowStat per scored row.
-constexpr size_t kWsHeader = 256;
+// Arguments of the row kernel.
+struct RowArgs {
+  SessIO io;                  // inputs (outputs unused) and the statistics
+  RowStat* stats;             // [total + B + total], writable view of io.stats
+  sdcp_row_stat* pub;         // optional public copy (statistics mode)
+  int stats_mode;             // 1: every row gets the full statistics
+  WsHeader* hdr;
+};
 
 int launch_row_stats(const RowArgs& a, int dtype, cudaStream_t stream);
-int launch_sessions(const SessArgs& a, int dtype, int cluster, bool pdl, cudaStream_t stream);
+int launch_sessions(const SessIO& a, int dtype, bool pdl, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------------
 // Order key of a binary32 bit pattern: unsigned order of keys = numeric order of the
@@ -223,134 +220,6 @@ __device__ __forceinline__ long long warp_sum_ll(long long v) {
   return v;
 }
 
-// Block-wide (kThreads) reductions through a small shared scratch; all threads get the
-// result.  Scratch must hold kWarps elements and is reused after a barrier.
-__device__ __forceinline__ float block_sum(float v, float* scratch) {
-  v = warp_reduce(v, [](float a, float b) { return a + b; });
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) scratch[w] = v;
-  __syncthreads();
-  float r = 0.f;
-  if (w == 0) {
-    r = (l < kWarps) ? scratch[l] : 0.f;
-    r = warp_reduce(r, [](float a, float b) { return a + b; });
-    if (l == 0) scratch[0] = r;
-  }
-  __syncthreads();
-  r = scratch[0];
-  return r;
-}
-__device__ __forceinline__ long long block_sum_ll(long long v, long long* scratch) {
-  v = warp_sum_ll(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) scratch[w] = v;
-  __syncthreads();
-  long long r = 0;
-  if (w == 0) {
-    r = (l < kWarps) ? scratch[l] : 0;
-    r = warp_sum_ll(r);
-    if (l == 0) scratch[0] = r;
-  }
-  __syncthreads();
-  r = scratch[0];
-  return r;
-}
-__device__ __forceinline__ int64_t block_max_i64(int64_t v, long long* scratch) {
-  v = warp_max_i64(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) scratch[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    int64_t r = (l < kWarps) ? (int64_t)scratch[l] : INT64_MIN;
-    r = warp_max_i64(r);
-    if (l == 0) scratch[0] = r;
-  }
-  __syncthreads();
-  return (int64_t)scratch[0];
-}
-__device__ __forceinline__ int64_t block_min_i64(int64_t v, long long* scratch) {
-  v = warp_min_i64(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) scratch[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    int64_t r = (l < kWarps) ? (int64_t)scratch[l] : INT64_MAX;
-    r = warp_min_i64(r);
-    if (l == 0) scratch[0] = r;
-  }
-  __syncthreads();
-  return (int64_t)scratch[0];
-}
-
-// Exclusive scan of one float per thread (block of kThreads), fixed association.
-// Returns the exclusive prefix; *total gets the sum over the block.
-__device__ __forceinline__ float block_exclusive_scan(float v, float* scratch, float* total) {
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  float incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    float t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (l >= o) incl += t;
-  }
-  __syncthreads();
-  if (l == 31) scratch[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    float s = (l < kWarps) ? scratch[l] : 0.f;
-    float si = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      float t = __shfl_up_sync(0xFFFFFFFFu, si, o);
-      if (l >= o) si += t;
-    }
-    float se = __shfl_up_sync(0xFFFFFFFFu, si, 1);
-    if (l < kWarps) scratch[kWarps + l] = (l == 0) ? 0.f : se;  // exclusive warp offsets
-    if (l == kWarps - 1) scratch[2 * kWarps] = si;
-  }
-  __syncthreads();
-  float excl_in_warp = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-  if (l == 0) excl_in_warp = 0.f;
-  float r = (w == 0) ? excl_in_warp : scratch[kWarps + w] + excl_in_warp;
-  *total = scratch[2 * kWarps];
-  return r;
-}
-// Same for 64-bit integers (exact).
-__device__ __forceinline__ long long block_exclusive_scan_ll(long long v, long long* scratch,
-                                                             long long* total) {
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  long long incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    long long t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (l >= o) incl += t;
-  }
-  __syncthreads();
-  if (l == 31) scratch[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    long long s = (l < kWarps) ? scratch[l] : 0;
-    long long si = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      long long t = __shfl_up_sync(0xFFFFFFFFu, si, o);
-      if (l >= o) si += t;
-    }
-    long long se = __shfl_up_sync(0xFFFFFFFFu, si, 1);
-    if (l < kWarps) scratch[kWarps + l] = (l == 0) ? 0 : se;
-    if (l == kWarps - 1) scratch[2 * kWarps] = si;
-  }
-  __syncthreads();
-  long long ew = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-  if (l == 0) ew = 0;
-  long long r = scratch[kWarps + w] + ew;
-  *total = scratch[2 * kWarps];
-  return r;
-}
-
 // Session of a row by a warp-cooperative 32-ary search over m_offsets: the largest b in
 // [0, B) with key(b) <= r, key(b) = m_offsets[b] + (target ? b : 0).  Clamped to [0, B).
 __device__ __forceinline__ int32_t find_session(const int32_t* __restrict__ m_offsets, int32_t B,
@@ -358,17 +227,14 @@ __device__ __forceinline__ int32_t find_session(const int32_t* __restrict__ m_of
   int64_t lo = 0, hi = B;
   const int l = threadIdx.x & 31;
   while (hi - lo > 1) {
-    int64_t step = (hi - lo + 31) / 32;
-    int64_t j = lo + (int64_t)l * step;
+    const int64_t step = (hi - lo + 31) / 32;
+    const int64_t j = lo + (int64_t)l * step;
     bool ok = false;
-    if (j < hi) {
-      int64_t k = (int64_t)__ldg(&m_offsets[j]) + (target ? j : 0);
-      ok = (k <= r);
-    }
-    unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
-    int last = (m == 0) ? 0 : (31 - __clz(m));
-    int64_t nlo = lo + (int64_t)last * step;
-    int64_t nhi = nlo + step;
+    if (j < hi) ok = (int64_t)__ldg(&m_offsets[j]) + (target ? j : 0) <= r;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
+    const int last = (m == 0) ? 0 : (31 - __clz(m));
+    const int64_t nlo = lo + (int64_t)last * step;
+    const int64_t nhi = nlo + step;
     lo = nlo;
     hi = nhi < hi ? nhi : hi;
   }
@@ -418,6 +284,10 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Named barrier 1 (the id is a literal, so a kernel reserves no other barrier for it).
+__device__ __forceinline__ void named_sync1(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
 // Programmatic dependent launch controls (no-ops when the launch did not enable them).
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -430,10 +300,11 @@ __device__ __forceinline__ void pdl_wait_primary() {
 // Reductions over a group of warps 0..nw-1 that share a named barrier (fixed order).
 // scratch needs 2 * 32 + 2 entries.
 // ---------------------------------------------------------------------------------
+// A group of warps 0 .. nthreads/32 - 1 of a CTA that synchronises on named barrier 1.
 struct Group {
   int nthreads;
-  int bar;
-  __device__ __forceinline__ void sync() const { named_sync(bar, nthreads); }
+  int bar;  // always 1
+  __device__ __forceinline__ void sync() const { named_sync1(nthreads); }
   __device__ __forceinline__ int nwarps() const { return nthreads >> 5; }
 };
 __device__ __forceinline__ float group_sum(const Group& g, float v, float* scratch) {

@@ -2,29 +2,29 @@
 // profile (SDCP draft draft-li-mlc-inference-acceleration-00, Section 4.1: temperature,
 // then top-k, then top-p; temperature 0 selects the argmax, ties to the smallest id).
 //
-// A persistent kernel, two CTAs per SM.  In each CTA one producer warp streams the rows the
-// CTA owns (rows blockIdx.x, blockIdx.x + gridDim.x, ...) from HBM into a ring of three
-// 32 KB shared-memory stages with bulk copies (TMA) that complete on mbarriers; eight
-// consumer warps reduce each stage as it lands (eight 16-byte vectors per thread) and hand
-// it back.  The HBM stream therefore does not wait for the per-row work (reductions,
-// thresholds, the statistics record): every logits byte is read from HBM once, and up to
-// 64 KB per CTA are in flight.
+// A persistent kernel, two CTAs per SM.  In each CTA one producer warp claims rows from a
+// grid-wide counter (so CTAs that meet slow rows take fewer) and streams each row from HBM
+// into a ring of three 32 KB shared-memory stages with bulk copies (TMA) that complete on
+// mbarriers; eight consumer warps reduce each stage as it lands (eight 16-byte vectors per
+// thread) and hand it back.  The HBM stream therefore does not wait for the per-row work:
+// every logits byte is read from HBM once, and up to 96 KB per CTA are in flight.
 //
 // Per row the consumers keep, per thread, the running maximum, its smallest id when the row
 // needs an argmax, and the sum of exp relative to it (online softmax) when it needs one;
 // warps merge in a fixed order, so every result is independent of scheduling.
 //
-// Top-k / top-p on bf16 rows: an exact-value histogram of the bf16 values within Dz nats
-// below the row maximum (8 for top-k, 11 for top-p, then twice that, then the 2048 values)
-// is built from a second read of the row (it was just streamed and sits in L2); only
-// vectors whose maximum reaches the window are looked at element by element (integer
-// shared-memory atomics: deterministic).  All tokens that share a bf16 value have the same
-// probability, so the mass of a bin is count * exp(v - max): the k-th token and the top-p
-// crossing come out of one scan over the bins.  A tie at the cut value is broken by id
-// after one more pass that collects the ids holding that value.  Rows no window decides
-// (fp32 logits with a filter, or a nucleus deeper than 2048 values) take a generic
-// bisection over the order-key space.
-#include "sdcp_device.cuh"
+// Top-k / top-p on bf16 rows: all tokens that share a bf16 value have the same
+// probability, so the exact count of every value in a window below the row maximum decides
+// both cuts (the mass of a value is count * exp(v - max)).  The window (Dz nats below the
+// maximum of the row's first stage: 8 for top-k, 11 for top-p) is counted while the row
+// streams, with a shared-memory histogram of up to 2048 values that every element updates
+// under a predicate (no divergence); one warp then scans the bins for the k-th token and
+// the top-p crossing.  A cut inside one value keeps its first tokens in id order; only
+// their number is recorded.  Rows the window cannot decide are searched again from L2
+// (wider windows, then a bisection over the order-key space).
+#include <climits>
+
+#include "sdcp_session.cuh"
 
 namespace sdcp {
 
@@ -37,11 +37,14 @@ constexpr int kChunk = 32768;            // bytes per ring stage (8 vectors per 
 constexpr int kConsBar = 1;              // named barrier of the consumer warps
 constexpr long long kWaitPolls = 1ll << 22;
 constexpr int kRowCtasPerSm = 2;
+constexpr int kVecPerThread = kChunk / 16 / kCons;
+static_assert(kCons == kThreads, "the consumer group runs session completions");
 
 struct RowPlan {
-  long long row_id;  // < 0: end of the CTA's work
+  long long row_id;  // < 0: no more work for the CTA
   int b;
   int nchunks;
+  int32_t xt;        // the row's draft token as the token array holds it (-1: none)
 };
 
 struct RowShared {
@@ -49,22 +52,23 @@ struct RowShared {
   uint64_t empty[kStages];
   RowPlan plan[kStages];
   volatile int abort;
-  int pad0;
-  // per-warp partials and the merged row result
+  // per-warp partials
   float w_fm[32], w_s[32];
   long long w_amax[32];
-  float r_lmax, r_s;
-  long long r_amax;
   float fscr[2 * 32 + 4];
   long long lscr[2 * 32 + 4];
-  // window histogram and the list of the window's tokens (value key, id)
+  // window of the row being streamed: bin d counts the tokens whose bf16 value key is
+  // win_top16 - d (d < win_nb); positive windows index bins by bit pattern, d = win_hih - h
+  float win_lo;
+  uint32_t win_top16;
+  int win_nb, win_on, win_pos, win_hih;
+  uint32_t xbits;  // the draft token's logit bits
+  // the merged row and its cut (warp 0 -> group)
+  float r_lmax, r_s, r_skept;
+  long long r_amax, r_thr_n;
+  uint32_t r_thr_key;
+  int r_kept, r_done, r_fallback;
   uint32_t hist[kWindowBins];
-  // window built while the row streams: anchored on the maximum of its first stage
-  float win_lo;            // lowest value in the window
-  uint32_t win_top16;      // bin i holds the bf16 value key win_top16 - i
-  int win_on, win_over;    // window in use; a token above the top was seen
-  int b_dk, b_tk, b_dp, b_np, b_found, b_cbefore;
-  float b_mbefore;
 };
 
 // --------------------------------------------------------------------------------------
@@ -109,7 +113,7 @@ __device__ __forceinline__ float vec_max(const uint4& q, __nv_bfloat16) {
 }
 
 template <typename T, bool ARGMAX, bool SUM>
-__device__ __forceinline__ void acc_vector(ThreadAcc& a, const uint4& q, long long id0, float c) {
+__device__ __forceinline__ float acc_vector(ThreadAcc& a, const uint4& q, long long id0, float c) {
   constexpr int E = Elem<T>::kPerVec;
   uint32_t b[E];
   Elem<T>::unpack(q, b);
@@ -135,21 +139,91 @@ __device__ __forceinline__ void acc_vector(ThreadAcc& a, const uint4& q, long lo
     for (int e = 0; e < E; ++e) t += ex2(fmaf(v[e], c, -a.fmc));
     a.s += t;
   }
+  return vm;
 }
 
-// Vectors [0, nv) of one ring stage; vector v is element id0 + v * E of the row.
-template <typename T, bool ARGMAX, bool SUM>
-__device__ __forceinline__ void acc_stage(ThreadAcc& a, const uint4* sv, int nv, long long id0, float c) {
+// --------------------------------------------------------------------------------------
+// Window histogram.  Every element of a bf16 row with a filter updates the bin of its value
+// under a predicate.  Positive windows (bottom above +0): with h the bf16 bit pattern as a
+// signed 16-bit number, value order is h order and d = win_hih - h is in [0, nb) exactly
+// for the window's values (negative values have h < 0, values above the top d < 0).
+// Other windows go through the order key: d = win_top16 - key16.
+// --------------------------------------------------------------------------------------
+template <bool POS>
+__device__ __forceinline__ void win_word(uint32_t* hist, uint32_t wd, uint32_t top, uint32_t nb) {
+  uint32_t d0, d1;
+  if (POS) {
+    d0 = top - (uint32_t)((int32_t)(wd << 16) >> 16);
+    d1 = top - (uint32_t)((int32_t)wd >> 16);
+  } else {
+    d0 = top - (order_key(wd << 16) >> 16);
+    d1 = top - (order_key(wd & 0xFFFF0000u) >> 16);
+  }
+  if (d0 < nb) atomicAdd(hist + d0, 1u);
+  if (d1 < nb) atomicAdd(hist + d1, 1u);
+}
+template <typename T, bool POS>
+__device__ __forceinline__ void win_vector(uint32_t* hist, const uint4& q, uint32_t top, uint32_t nb) {
+  if constexpr (sizeof(T) == 2) {
+    win_word<POS>(hist, q.x, top, nb);
+    win_word<POS>(hist, q.y, top, nb);
+    win_word<POS>(hist, q.z, top, nb);
+    win_word<POS>(hist, q.w, top, nb);
+  }
+}
+// One element (bits of a bf16 value in the upper half) of the row's unaligned ends.
+__device__ __forceinline__ void win_scalar(RowShared& sh, uint32_t bits) {
+  const uint32_t d = sh.win_top16 - (order_key(bits) >> 16);
+  if (d < (uint32_t)sh.win_nb) atomicAdd(sh.hist + d, 1u);
+}
+
+// Vectors [0, nv) of one ring stage (nv <= kVecPerThread * kCons); vector v is element
+// id0 + v * E of the row and belongs to consumer thread v % kCons.  WIN 1 / 2: count the
+// stage into the window (positive / general indexing).  Vectors past nv read as -inf, which
+// changes no statistic and no bin.
+template <typename T, bool ARGMAX, bool SUM, int WIN>
+__device__ __forceinline__ void acc_stage(ThreadAcc& a, RowShared& sh, const uint4* sv, int nv,
+                                          long long id0, float c) {
   constexpr int E = Elem<T>::kPerVec;
-  int v = threadIdx.x;
-  for (; v + 3 * kCons < nv; v += 4 * kCons) {
+  const int t = threadIdx.x;
+  const uint32_t top = (WIN == 1) ? (uint32_t)sh.win_hih : sh.win_top16;
+  const uint32_t nb = (uint32_t)sh.win_nb;
+  const uint32_t ninf = (sizeof(T) == 2) ? 0xFF80FF80u : 0xFF800000u;
+  const uint4 pad = make_uint4(ninf, ninf, ninf, ninf);
+#pragma unroll 1
+  for (int i0 = 0; i0 < kVecPerThread; i0 += 4) {
     uint4 q[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) q[u] = sv[v + u * kCons];
+    for (int u = 0; u < 4; ++u) {
+      const int v = t + (i0 + u) * kCons;
+      q[u] = (v < nv) ? sv[v] : pad;
+    }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc_vector<T, ARGMAX, SUM>(a, q[u], id0 + (long long)(v + u * kCons) * E, c);
+    for (int u = 0; u < 4; ++u) {
+      const int v = t + (i0 + u) * kCons;
+      acc_vector<T, ARGMAX, SUM>(a, q[u], id0 + (long long)v * E, c);
+      if (WIN == 1) win_vector<T, true>(sh.hist, q[u], top, nb);
+      if (WIN == 2) win_vector<T, false>(sh.hist, q[u], top, nb);
+    }
   }
-  for (; v < nv; v += kCons) acc_vector<T, ARGMAX, SUM>(a, sv[v], id0 + (long long)v * E, c);
+}
+
+// The window over a stage that was reduced before the window was placed (the first).
+template <typename T>
+__device__ __forceinline__ void window_stage(RowShared& sh, const uint4* sv, int nv) {
+  const int t = threadIdx.x;
+  const bool pos = sh.win_pos != 0;
+  const uint32_t top = pos ? (uint32_t)sh.win_hih : sh.win_top16;
+  const uint32_t nb = (uint32_t)sh.win_nb;
+#pragma unroll 4
+  for (int i = 0; i < kVecPerThread; ++i) {
+    const int v = t + i * kCons;
+    if (v < nv) {
+      const uint4 q = sv[v];
+      if (pos) win_vector<T, true>(sh.hist, q, top, nb);
+      else win_vector<T, false>(sh.hist, q, top, nb);
+    }
+  }
 }
 
 template <typename T, bool ARGMAX, bool SUM>
@@ -161,14 +235,14 @@ __device__ __forceinline__ void acc_scalars(ThreadAcc& a, const T* row, const Ro
 // Row modes: which statistics a row needs.
 enum RowMode { kModeMax = 0, kModeArgmax = 1, kModeSum = 2, kModeArgmaxSum = 3 };
 
-template <typename T>
-__device__ __forceinline__ void acc_stage_mode(int mode, ThreadAcc& a, const uint4* sv, int nv,
+template <typename T, int WIN>
+__device__ __forceinline__ void acc_stage_mode(int mode, ThreadAcc& a, RowShared& sh, const uint4* sv, int nv,
                                                long long id0, float c) {
   switch (mode) {
-    case kModeMax: acc_stage<T, false, false>(a, sv, nv, id0, c); break;
-    case kModeArgmax: acc_stage<T, true, false>(a, sv, nv, id0, c); break;
-    case kModeSum: acc_stage<T, false, true>(a, sv, nv, id0, c); break;
-    default: acc_stage<T, true, true>(a, sv, nv, id0, c); break;
+    case kModeMax: acc_stage<T, false, false, WIN>(a, sh, sv, nv, id0, c); break;
+    case kModeArgmax: acc_stage<T, true, false, WIN>(a, sh, sv, nv, id0, c); break;
+    case kModeSum: acc_stage<T, false, true, WIN>(a, sh, sv, nv, id0, c); break;
+    default: acc_stage<T, true, true, WIN>(a, sh, sv, nv, id0, c); break;
   }
 }
 template <typename T>
@@ -197,18 +271,18 @@ struct RowCtx {
 
 __device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, int b, bool bf16) {
   RowCtx x;
-  const long long R_T = A.total + A.B;
+  const long long R_T = A.io.total + A.io.B;
   x.is_target = row_id < R_T;
   x.b = b;
-  x.P = A.params[b];
-  const long long off0 = A.m_offsets[b], off1 = A.m_offsets[b + 1];
+  x.P = A.io.params[b];
+  const long long off0 = A.io.m_offsets[b], off1 = A.io.m_offsets[b + 1];
   const long long M = off1 - off0;
   const long long pos = x.is_target ? row_id - off0 - b : (row_id - R_T) - off0;
   x.tok_idx = x.is_target ? row_id - b : row_id - R_T;
-  x.has_x = (pos >= 0 && pos < M && x.tok_idx >= 0 && x.tok_idx < A.total);
+  x.has_x = (pos >= 0 && pos < M && x.tok_idx >= 0 && x.tok_idx < A.io.total);
   const bool params_ok = (x.P.top_p_milli <= 1000u);
   const bool session_ok = params_ok && (x.P.rule_id == 1u || x.P.rule_id == 2u) && M >= 1 &&
-                          M <= SDCP_MAX_M && off0 >= 0 && off1 <= A.total;
+                          M <= SDCP_MAX_M && off0 >= 0 && off1 <= A.io.total;
   bool want_argmax, want_profile;
   if (A.stats_mode) {
     x.skip = !params_ok;
@@ -216,7 +290,7 @@ __device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, in
     want_profile = true;
   } else {
     const bool rule2 = (x.P.rule_id == 2u);
-    x.skip = !session_ok || (!x.is_target && !rule2) || (!x.is_target && A.draft == nullptr);
+    x.skip = !session_ok || (!x.is_target && !rule2) || (!x.is_target && A.io.draft == nullptr);
     want_argmax = !rule2 || x.P.temperature_milli == 0u;
     want_profile = rule2 && x.P.temperature_milli != 0u;
   }
@@ -224,7 +298,7 @@ __device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, in
   x.one_hot = (tm == 0u);
   x.scale_d = x.one_hot ? 0.0 : 1000.0 / (double)tm;
   x.c = (float)(x.scale_d * 1.4426950408889634);  // log2(e) * 1000/T
-  x.topk = !x.one_hot && want_profile && x.P.top_k != 0u && (int64_t)x.P.top_k < A.V;
+  x.topk = !x.one_hot && want_profile && x.P.top_k != 0u && (int64_t)x.P.top_k < A.io.V;
   x.topp = !x.one_hot && want_profile && x.P.top_p_milli < 1000u;
   x.need_keys = want_argmax || x.one_hot;  // the argmax is needed
   x.need_sum = want_profile && !x.one_hot && !x.topk;
@@ -236,9 +310,9 @@ __device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, in
 
 template <typename T>
 __device__ __forceinline__ const T* row_ptr(const RowArgs& A, long long row_id) {
-  const long long R_T = A.total + A.B;
-  const T* base = reinterpret_cast<const T*>(row_id < R_T ? A.target : A.draft);
-  return base + (row_id < R_T ? row_id : row_id - R_T) * A.V;
+  const long long R_T = A.io.total + A.io.B;
+  const T* base = reinterpret_cast<const T*>(row_id < R_T ? A.io.target : A.io.draft);
+  return base + (row_id < R_T ? row_id : row_id - R_T) * A.io.V;
 }
 
 __device__ __forceinline__ void write_skipped(const RowArgs& A, long long row_id) {
@@ -354,119 +428,131 @@ struct Thresholds {
   bool fallback;
 };
 
-// Exact-value window selection from sh.hist, where bin i counts the tokens whose bf16 value
-// key is top16 - i (bins [0, nb)).  Returns false when the window cannot decide (fewer than
-// k tokens in it, or less mass than the nucleus needs).  A cut inside a value keeps the
-// first tokens of that value in id order; only their number is recorded here (all of them
-// have the same probability), the id bound is found where it is needed.
-__device__ bool select_from_hist(const Group& g, RowShared& sh, const RowCtx& x, float lmax,
-                                 float s_all, uint32_t top16, int nb, Thresholds& out) {
-  const int t = threadIdx.x;
-  // consumer thread t owns bins [BPT t, BPT t + BPT), in descending value order
-  constexpr int BPT = (kWindowBins + kCons - 1) / kCons;
-  long long cnt_t = 0;
-  float e1[BPT];
-  uint32_t cn[BPT];
-#pragma unroll
-  for (int i = 0; i < BPT; ++i) {
-    const int d = t * BPT + i;
-    cn[i] = (d < nb) ? sh.hist[d] : 0u;
-    const float v = key_value((top16 - (uint32_t)min(d, nb - 1)) << 16);
-    e1[i] = (cn[i] != 0u) ? ex2((v - lmax) * x.c) : 0.f;
-    cnt_t += cn[i];
+// Exact-value selection by one warp from hist, where bin d counts the tokens whose bf16
+// value key is top16 - d (d < nb, descending values).  Lane l owns bins [l bpl, l bpl +
+// bpl).  Returns false when the window cannot decide (fewer than k tokens in it, or less
+// mass than the nucleus needs).  A cut inside a value keeps the first tokens of that value
+// in id order; only their number is recorded (all of them have the same probability).
+__device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint32_t* hist,
+                            uint32_t top16, int nb, Thresholds& out) {
+  const int l = threadIdx.x & 31;
+  const int bpl = (nb + 31) >> 5;
+  const int d0 = min(nb, l * bpl), d1 = min(nb, d0 + bpl);
+  auto e_of = [&](int d) { return ex2((key_value((top16 - (uint32_t)d) << 16) - lmax) * x.c); };
+  long long cnt = 0;
+  float mass = 0.f;
+  for (int d = d0; d < d1; ++d) {
+    const uint32_t c = hist[d];
+    if (c != 0u) { cnt += c; mass += (float)c * e_of(d); }
   }
-  long long cnt_tot;
-  const long long cnt_ex = group_excl_scan_ll(g, cnt_t, sh.lscr, &cnt_tot);
-  int dk = INT_MAX, tk = 0;
+  // exclusive prefixes over the lanes (bins before the lane's first)
+  long long ci = cnt;
+  float mi = mass;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long tc = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+    const float tm = __shfl_up_sync(0xFFFFFFFFu, mi, o);
+    if (l >= o) { ci += tc; mi += tm; }
+  }
+  long long cpre = __shfl_up_sync(0xFFFFFFFFu, ci, 1);
+  float mpre = __shfl_up_sync(0xFFFFFFFFu, mi, 1);
+  if (l == 0) { cpre = 0; mpre = 0.f; }
+  int dk = nb, tk = 0;
+  float s_base = s_all;  // mass of the set the nucleus is taken from
+  const long long k = x.P.top_k;
   if (x.topk) {
-    const long long k = x.P.top_k;
-    if (t == 0) { sh.b_dk = -1; sh.b_tk = 0; }
-    g.sync();
-    if (cnt_ex < k && k <= cnt_ex + cnt_t) {
-      long long cc = cnt_ex;
-      for (int i = 0; i < BPT; ++i) {
-        if (cc + cn[i] >= k) { sh.b_dk = t * BPT + i; sh.b_tk = (int)(k - cc); break; }
-        cc += cn[i];
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, cpre < k && k <= cpre + cnt);
+    if (m == 0u) return false;  // fewer than k tokens in the window
+    const int src = __ffs(m) - 1;
+    int my_dk = 0, my_tk = 0;
+    float my_s = 0.f;
+    if (l == src) {
+      long long cc = cpre;
+      float mm = mpre;
+      for (int d = d0; d < d1; ++d) {
+        const uint32_t c = hist[d];
+        if (c == 0u) continue;
+        const float e = e_of(d);
+        if (cc + c >= k) { my_dk = d; my_tk = (int)(k - cc); my_s = mm + (float)my_tk * e; break; }
+        cc += c;
+        mm += (float)c * e;
       }
     }
-    g.sync();
-    dk = sh.b_dk;
-    tk = sh.b_tk;
-    g.sync();
-    if (dk < 0) return false;  // fewer than k tokens in the window
+    dk = __shfl_sync(0xFFFFFFFFu, my_dk, src);
+    tk = __shfl_sync(0xFFFFFFFFu, my_tk, src);
+    s_base = __shfl_sync(0xFFFFFFFFu, my_s, src);
   }
-  float m_t = 0.f;
-  float mb[BPT];
-#pragma unroll
-  for (int i = 0; i < BPT; ++i) {
-    const int d = t * BPT + i;
-    float m = 0.f;
-    if (!x.topk || d < dk) m = (float)cn[i] * e1[i];
-    else if (d == dk) m = (float)tk * e1[i];
-    mb[i] = m;
-    m_t += m;
-  }
-  float m_tot;
-  const float m_ex = group_excl_scan(g, m_t, sh.fscr, &m_tot);
-  const float s_base = x.topk ? m_tot : s_all;
-  int my_d = INT_MAX, my_n = 0;
-  float my_before = 0.f;
-  long long my_cbefore = 0;
+  int dcut = dk, ncut = tk;
   if (x.topp) {
     const float target = (float)((double)x.P.top_p_milli / 1000.0 * (double)s_base);
-    float cum = m_ex;
-    long long cc = cnt_ex;
-    for (int i = 0; i < BPT; ++i) {
-      const int d = t * BPT + i;
-      if (x.topk && d > dk) break;
-      const float nxt = cum + mb[i];
-      if (mb[i] > 0.f && nxt >= target) {
-        const long long avail = (x.topk && d == dk) ? tk : (long long)cn[i];
-        long long n = (long long)ceil(((double)target - (double)cum) / (double)e1[i]);
+    int cd = -1, cn = 0;
+    float cb = 0.f;
+    long long ccb = 0;
+    float cum = mpre;
+    long long cc = cpre;
+    for (int d = d0; d < d1 && d <= dk; ++d) {
+      const uint32_t c = hist[d];
+      if (c == 0u) continue;
+      const float e = e_of(d);
+      const long long avail = (x.topk && d == dk) ? tk : (long long)c;
+      const float md = (float)avail * e;
+      const float nxt = cum + md;
+      if (md > 0.f && nxt >= target) {
+        long long n = (long long)ceil(((double)target - (double)cum) / (double)e);
         if (n < 1) n = 1;
         if (n > avail) n = avail;
-        my_d = d; my_n = (int)n; my_before = cum; my_cbefore = cc;
+        cd = d; cn = (int)n; cb = cum; ccb = cc;
         break;
       }
       cum = nxt;
-      cc += cn[i];
+      cc += c;
     }
-  }
-  const int best = x.topp ? (int)group_min_i64(g, my_d, sh.lscr) : INT_MAX;
-  if (t == 0) sh.b_found = 0;
-  g.sync();
-  if (best != INT_MAX && my_d == best) {
-    sh.b_dp = best; sh.b_np = my_n; sh.b_mbefore = my_before; sh.b_cbefore = (int)my_cbefore;
-    sh.b_found = 1;
-  }
-  g.sync();
-  int dcut, ncut;
-  if (x.topp && sh.b_found) {
-    dcut = sh.b_dp;
-    ncut = sh.b_np;
-    const float e1c = ex2((key_value((top16 - (uint32_t)dcut) << 16) - lmax) * x.c);
-    out.s_kept = sh.b_mbefore + (float)ncut * e1c;
-    out.kept = sh.b_cbefore + ncut;
-  } else if (x.topk) {
-    dcut = dk;
-    ncut = tk;
-    out.s_kept = m_tot;
-    out.kept = (int)x.P.top_k;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, cd >= 0);
+    if (m != 0u) {
+      const int src = __ffs(m) - 1;
+      dcut = __shfl_sync(0xFFFFFFFFu, cd, src);
+      ncut = __shfl_sync(0xFFFFFFFFu, cn, src);
+      cb = __shfl_sync(0xFFFFFFFFu, cb, src);
+      ccb = __shfl_sync(0xFFFFFFFFu, ccb, src);
+      out.s_kept = cb + (float)ncut * e_of(dcut);
+      out.kept = (int)(ccb + ncut);
+    } else if (x.topk) {  // rounding kept the crossing out of reach: the whole top-k set
+      out.s_kept = s_base;
+      out.kept = (int)k;
+    } else {
+      return false;  // the nucleus reaches below the window
+    }
   } else {
-    g.sync();
-    return false;  // the nucleus reaches below the window
+    out.s_kept = s_base;
+    out.kept = (int)k;
   }
-  const uint32_t cut16 = top16 - (uint32_t)dcut;
-  const uint32_t ccut = sh.hist[dcut];
-  g.sync();
-  out.thr_key = cut16 << 16;
+  const uint32_t ccut = hist[dcut];
+  out.thr_key = (top16 - (uint32_t)dcut) << 16;
   out.thr_n = ((uint32_t)ncut >= ccut) ? LLONG_MAX : ncut;
   out.fallback = false;
   return true;
 }
 
+// Publishes a warp-0 result to the group (through sh.r_*).
+__device__ __forceinline__ void put_thresholds(RowShared& sh, bool done, const Thresholds& th) {
+  sh.r_done = done ? 1 : 0;
+  sh.r_thr_key = th.thr_key;
+  sh.r_thr_n = th.thr_n;
+  sh.r_kept = th.kept;
+  sh.r_skept = th.s_kept;
+  sh.r_fallback = th.fallback ? 1 : 0;
+}
+__device__ __forceinline__ bool get_thresholds(const RowShared& sh, Thresholds& th) {
+  th.thr_key = sh.r_thr_key;
+  th.thr_n = sh.r_thr_n;
+  th.kept = sh.r_kept;
+  th.s_kept = sh.r_skept;
+  th.fallback = sh.r_fallback != 0;
+  return sh.r_done != 0;
+}
+
 // Window histogram of the tokens within dz nats below the row maximum (dz = 0: the 2048
-// values below it), from a pass over the row in L2, then the selection.
+// values below it), from a pass over the row in L2, then the selection (group).
 template <typename T>
 __device__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
                                   const RowCtx& x, int64_t V, float lmax, float s_all, float dz,
@@ -484,10 +570,9 @@ __device__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, c
       if (klo16 < kmax16 && (int64_t)(kmax16 - klo16 + 1) < nb) nb = (int)(kmax16 - klo16 + 1);
     }
   }
+  g.sync();  // earlier readers of the histogram are done
   for (int i = t; i < kWindowBins; i += kCons) sh.hist[i] = 0u;
   g.sync();
-  // tokens with a value >= the window's lowest value go into the histogram; only vectors
-  // whose maximum reaches the window are looked at element by element
   const uint32_t klo16 = kmax16 - (uint32_t)(nb - 1);
   const float wbot = key_value(klo16 << 16);
   scan_row<T>(row, L, V, [&](const uint32_t (&b)[Elem<T>::kPerVec], long long id0, int n) {
@@ -500,47 +585,14 @@ __device__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, c
     }
   });
   g.sync();
-  return select_from_hist(g, sh, x, lmax, s_all, kmax16, nb, out);
-}
-
-// One token for the window built while the row streams.
-__device__ __forceinline__ void window_add(RowShared& sh, uint32_t bits) {
-  const uint32_t k16 = order_key(bits) >> 16;
-  if (k16 > sh.win_top16) sh.win_over = 1;
-  else atomicAdd(&sh.hist[sh.win_top16 - k16], 1u);
-}
-
-// Bits of element e of a 16-byte vector, e in [0, E) (no dynamic register indexing).
-__device__ __forceinline__ uint32_t vec_elem(const uint4& q, int e, float) {
-  return (e & 2) ? ((e & 1) ? q.w : q.z) : ((e & 1) ? q.y : q.x);
-}
-__device__ __forceinline__ uint32_t vec_elem(const uint4& q, int e, __nv_bfloat16) {
-  const uint32_t w = (e & 4) ? ((e & 2) ? q.w : q.z) : ((e & 2) ? q.y : q.x);
-  return (e & 1) ? (w & 0xFFFF0000u) : (w << 16);
-}
-
-// The window part of one ring stage: only vectors whose maximum reaches win_lo are looked
-// at, and in those only the elements that reach it (a bit mask walked with find-first-set).
-template <typename T>
-__device__ __forceinline__ void window_stage(RowShared& sh, const uint4* sv, int nv) {
-  constexpr int E = Elem<T>::kPerVec;
-  const float lo = sh.win_lo;
-  const uint32_t top16 = sh.win_top16;
-  for (int v = threadIdx.x; v < nv; v += kCons) {
-    const uint4 q = sv[v];
-    if (vec_max(q, T()) >= lo) {
-      uint32_t m = 0u;
-#pragma unroll
-      for (int e = 0; e < E; ++e) m |= (__uint_as_float(vec_elem(q, e, T())) >= lo ? 1u : 0u) << e;
-      while (m) {
-        const int e = __ffs(m) - 1;
-        m &= m - 1u;
-        const uint32_t k16 = order_key(vec_elem(q, e, T())) >> 16;
-        if (k16 > top16) sh.win_over = 1;
-        else atomicAdd(&sh.hist[top16 - k16], 1u);
-      }
-    }
+  if ((t >> 5) == 0) {
+    Thresholds th = out;
+    const bool done = warp_select(x, lmax, s_all, sh.hist, kmax16, nb, th);
+    if ((t & 31) == 0) put_thresholds(sh, done, th);
   }
+  g.sync();
+  const bool done = get_thresholds(sh, out);
+  return done;
 }
 
 // Generic search: bisection over the order-key space with group-wide reductions.
@@ -625,27 +677,56 @@ __device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, 
   }
 }
 
+// Tokens with order key `key` and an id below xt (group; second read of the row, from L2).
+template <typename T>
+__device__ long long count_key_before(const Group& g, RowShared& sh, const T* row, int64_t xt, uint32_t key) {
+  const bool al = ((uintptr_t)row & 15u) == 0;
+  long long c = 0;
+#pragma unroll 4
+  for (int64_t j0 = (int64_t)threadIdx.x * kEpt; j0 < xt; j0 += (int64_t)kCons * kEpt) {
+    Raw8<T> r;
+    load_raw8<T>(row, al, xt, j0, r);
+    uint32_t b[kEpt];
+    unpack_raw8<T>(r, b);
+#pragma unroll
+    for (int e = 0; e < kEpt; ++e) c += (j0 + e < xt && order_key(b[e]) == key) ? 1 : 0;
+  }
+  return group_sum_ll(g, c, sh.lscr);
+}
+
 // --------------------------------------------------------------------------------------
 // Consumers: finish one row after its stages were reduced.
 // --------------------------------------------------------------------------------------
 template <typename T>
-__device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, long long row_id,
+__device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, const RowPlan& plan,
                            ThreadAcc& acc) {
   const Group g{kCons, kConsBar};
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
-  const int64_t V = A.V;
+  const int64_t V = A.io.V;
+  const long long row_id = plan.row_id;
   const T* row = row_ptr<T>(A, row_id);
   const RowLayout L = row_layout(row, V);
   acc_scalars_mode<T>(x.mode, acc, row, L, V, x.c);
-
-  // warp merge (fixed butterfly), then thread 0 merges the warps in order
+  if (x.window && sh.win_on) {  // the row's unaligned ends go into the window too
+    for (int64_t j = t; j < L.head; j += kCons) win_scalar(sh, load_bits(row, j));
+    for (int64_t j = L.tail0 + t; j < V; j += kCons) win_scalar(sh, load_bits(row, j));
+  }
+  // warp merge (fixed butterfly), then the warps in order
   const float wfm = warp_reduce(acc.fm, [](float a, float b) { return fmax_nan(a, b); });
   const float mine = (acc.s == 0.f || acc.fm == -INFINITY) ? 0.f : acc.s * ex2((acc.fm - wfm) * x.c);
   const float ws = x.need_sum ? warp_reduce(mine, [](float a, float b) { return a + b; }) : 0.f;
   const long long wam = warp_min_i64(acc.fm == wfm ? acc.amax : LLONG_MAX);
   if (l == 0) { sh.w_fm[w] = wfm; sh.w_s[w] = ws; sh.w_amax[w] = wam; }
-  g.sync();
-  if (t == 0) {
+  g.sync();  // partials and the window histogram are complete
+  const bool filt = x.topk || x.topp;
+  auto is_bad = [&](float lm, float s) {
+    return (lm != lm || lm == INFINITY || lm == -INFINITY) || (x.need_sum && !(s < INFINITY));
+  };
+  float lmax = 0.f, s_all = 0.f;
+  long long amax = LLONG_MAX;
+  Thresholds th{0u, LLONG_MAX, (int)V, 0.f, false};
+  bool done = false;
+  if (w == 0) {  // the merged row (every lane of warp 0), and the window's cut
     float fm = -INFINITY;
     for (int i = 0; i < kConsWarps; ++i) fm = fmax_nan(fm, sh.w_fm[i]);
     float s = 0.f;
@@ -654,120 +735,123 @@ __device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, lon
       if (x.need_sum && sh.w_s[i] != 0.f && sh.w_fm[i] != -INFINITY) s += sh.w_s[i] * ex2((sh.w_fm[i] - fm) * x.c);
       if (sh.w_fm[i] == fm) am = min(am, (long long)sh.w_amax[i]);
     }
-    sh.r_lmax = fm; sh.r_s = s; sh.r_amax = am;
+    lmax = fm; s_all = s; amax = am;
+    th.s_kept = s_all;
+    if (filt && !is_bad(lmax, s_all) && x.window && sh.win_on) {
+      const uint32_t kmax16 = order_key(__float_as_uint(lmax)) >> 16;
+      const uint32_t top16 = sh.win_top16, lo16 = top16 - (uint32_t)(sh.win_nb - 1);
+      if (kmax16 >= lo16 && kmax16 <= top16)
+        done = warp_select(x, lmax, s_all, sh.hist + (top16 - kmax16), kmax16, (int)(kmax16 - lo16 + 1), th);
+    }
+    if (filt && l == 0) { sh.r_lmax = lmax; sh.r_s = s_all; sh.r_amax = amax; put_thresholds(sh, done, th); }
   }
-  g.sync();
-  const float lmax = sh.r_lmax;
-  const float s_all = sh.r_s;
-  const long long amax = sh.r_amax;
-  // no distribution: NaN, +inf, or no finite logit
-  int bad = (lmax != lmax || lmax == INFINITY || lmax == -INFINITY) ? 1 : 0;
-  if (x.need_sum && !(s_all < INFINITY)) bad = 1;
+  if (filt) {  // the group takes the cut (and searches again where the window did not decide)
+    g.sync();
+    lmax = sh.r_lmax; s_all = sh.r_s; amax = sh.r_amax;
+    done = get_thresholds(sh, th);
+    if (!is_bad(lmax, s_all) && !done) {
+      th = Thresholds{0u, LLONG_MAX, (int)V, s_all, false};
+      if (sizeof(T) == 2) {
+        // the k-th token of top-k lies a few nats below the maximum, the top-p crossing of
+        // a broad distribution deeper
+        const float dz1 = x.topp ? 11.f : 8.f;
+        done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, dz1, th);
+        if (!done) done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, 2.f * dz1, th);
+        if (!done) done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, 0.f, th);
+      }
+      if (!done) generic_thresholds<T>(g, sh, row, L, x, V, lmax, order_key(__float_as_uint(lmax)), th);
+    }
+  }
+  const bool bad = is_bad(lmax, s_all);  // exact in warp 0 and, for filtered rows, everywhere
   const uint32_t kmax = order_key(__float_as_uint(lmax));
-  const uint32_t kmax_f = kmax;
-
-  Thresholds th{0u, LLONG_MAX, (int)V, s_all, false};
-  const bool filters = (x.topk || x.topp) && !bad;
-  if (filters) {
-    bool done = false;
-    if (x.window && sh.win_on) {
-      // the window built while the row streamed, plus the row's unaligned ends
-      const float lo = sh.win_lo;
-      for (int64_t j = t; j < L.head; j += kCons) {
-        const uint32_t bits = load_bits(row, j);
-        if (__uint_as_float(bits) >= lo) window_add(sh, bits);
-      }
-      for (int64_t j = L.tail0 + t; j < V; j += kCons) {
-        const uint32_t bits = load_bits(row, j);
-        if (__uint_as_float(bits) >= lo) window_add(sh, bits);
-      }
-      g.sync();
-      const bool usable = !sh.win_over && (order_key(__float_as_uint(lmax)) >> 16) <= sh.win_top16;
-      const uint32_t top16 = sh.win_top16;
-      g.sync();
-      if (usable) done = select_from_hist(g, sh, x, lmax, s_all, top16, kWindowBins, th);
-    }
-    if (sizeof(T) == 2 && !done) {
-      // first window: the k-th token of top-k lies a few nats below the maximum, the top-p
-      // crossing of a broad distribution deeper
-      const float dz1 = x.topp ? 11.f : 8.f;
-      done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, dz1, th);
-      if (!done) done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, 2.f * dz1, th);
-      if (!done) done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, 0.f, th);
-    }
-    if (!done) generic_thresholds<T>(g, sh, row, L, x, V, lmax, kmax_f, th);
-  }
-  // the draft token of the row: kept?  (Rank among the tokens of the cut value when the cut
-  // falls inside that value; rare, so it is counted here over the ids before it.)
+  const bool filters = filt && !bad;
   uint32_t thr_key = 0u;
   long long thr_n = LLONG_MAX;
   if (x.one_hot) { thr_key = kmax; thr_n = 1; }
   else if (filters) { thr_key = th.thr_key; thr_n = th.thr_n; }
+  // the draft token of the row: kept?  (Its rank among the tokens of the cut value when the
+  // cut falls inside that value; counted over the ids before it.)
   int32_t xt = -1;
   uint32_t xb = 0u;
   bool kept_x = false;
   if (x.has_x && !bad) {
-    xt = A.tokens[x.tok_idx];
+    xt = plan.xt;
     if (xt >= 0 && (int64_t)xt < V) {
-      xb = load_bits(row, xt);
+      xb = sh.xbits;
       const uint32_t xk = order_key(xb);
-      if (x.one_hot) {
-        kept_x = (xt == amax);
-      } else if (xk > thr_key) {
-        kept_x = true;
-      } else if (xk == thr_key) {
-        if (thr_n == LLONG_MAX) {
-          kept_x = true;
-        } else {
-          long long before = 0;
-          for (int64_t j = t; j < xt; j += kCons) before += (order_key(load_bits(row, j)) == thr_key) ? 1 : 0;
-          kept_x = group_sum_ll(g, before, sh.lscr) < thr_n;
-        }
-      }
+      if (x.one_hot) kept_x = (xt == amax);
+      else if (xk > thr_key) kept_x = true;
+      else if (xk == thr_key) kept_x = (thr_n == LLONG_MAX) || count_key_before<T>(g, sh, row, xt, thr_key) < thr_n;
     } else {
       xt = -2;  // out of range: reported through the session status
     }
   }
+  if (t == 0) {
+    uint32_t flags = bad ? SDCP_ROW_INVALID : 0u;
+    if (filters && th.fallback) flags |= SDCP_ROW_FALLBACK;
+    RowStat st;
+    st.lmax = lmax;
+    st.argmax = (amax == LLONG_MAX) ? -1 : (int32_t)amax;
+    st.thr_key = thr_key;
+    st.thr_n = (thr_n == LLONG_MAX) ? INT_MAX : (int32_t)thr_n;
+    if (x.one_hot) {
+      st.s = 1.f; st.kept = 1;
+    } else if (filters) {
+      st.s = th.s_kept; st.kept = th.kept;
+    } else {
+      st.s = s_all; st.kept = (int32_t)V;
+    }
+    st.dlx = __int_as_float(0x7FC00000);
+    if (xt >= 0) {
+      flags |= kRowHasX;
+      const float lx = __uint_as_float(xb);
+      st.dlx = lx - lmax;
+      if (kept_x && lx != -INFINITY) flags |= SDCP_ROW_X_KEPT;
+    }
+    st.flags = flags;
+    A.stats[row_id] = st;
+    if (A.pub) {
+      sdcp_row_stat q;
+      q.lmax = st.lmax;
+      q.log_s = bad ? __int_as_float(0x7FC00000) : (float)log((double)st.s);
+      q.argmax = st.argmax;
+      q.kept = st.kept;
+      q.thr_key = st.thr_key;
+      q.thr_n = st.thr_n;
+      q.flags = flags & ~kRowHasX;
+      if (!(flags & kRowHasX)) q.lp_x = __int_as_float(0x7FC00000);
+      else if (!(flags & SDCP_ROW_X_KEPT)) q.lp_x = -INFINITY;
+      else if (x.one_hot) q.lp_x = 0.f;
+      else q.lp_x = (float)((double)st.dlx * x.scale_d - log((double)st.s));
+      A.pub[row_id] = q;
+    }
+  }
   g.sync();  // shared scratch of this row is free again after this point
-  if (t != 0) return;
-  uint32_t flags = bad ? SDCP_ROW_INVALID : 0u;
-  if (filters && th.fallback) flags |= SDCP_ROW_FALLBACK;
-  RowStat st;
-  st.lmax = lmax;
-  st.argmax = (amax == LLONG_MAX) ? -1 : (int32_t)amax;
-  st.thr_key = thr_key;
-  st.thr_n = (thr_n == LLONG_MAX) ? INT_MAX : (int32_t)thr_n;
-  if (x.one_hot) {
-    st.s = 1.f; st.kept = 1;
-  } else if (filters) {
-    st.s = th.s_kept; st.kept = th.kept;
-  } else {
-    st.s = s_all; st.kept = (int32_t)V;
-  }
-  st.dlx = __int_as_float(0x7FC00000);
-  if (xt >= 0) {
-    flags |= kRowHasX;
-    const float lx = __uint_as_float(xb);
-    st.dlx = lx - lmax;
-    if (kept_x && lx != -INFINITY) flags |= SDCP_ROW_X_KEPT;
-  }
-  st.flags = flags;
-  A.stats[row_id] = st;
-  if (A.pub) {
-    sdcp_row_stat q;
-    q.lmax = st.lmax;
-    q.log_s = bad ? __int_as_float(0x7FC00000) : (float)log((double)st.s);
-    q.argmax = st.argmax;
-    q.kept = st.kept;
-    q.thr_key = st.thr_key;
-    q.thr_n = st.thr_n;
-    q.flags = flags & ~kRowHasX;
-    if (!(flags & kRowHasX)) q.lp_x = __int_as_float(0x7FC00000);
-    else if (!(flags & SDCP_ROW_X_KEPT)) q.lp_x = -INFINITY;
-    else if (x.one_hot) q.lp_x = 0.f;
-    else q.lp_x = (float)((double)st.dlx * x.scale_d - log((double)st.s));
-    A.pub[row_id] = q;
-  }
+}
+
+// A row claimed by the producer warp.
+struct SlotInfo {
+  long long row_id;  // -1: none
+  int b;
+  bool skip;
+  int32_t xt;        // the row's draft token (-1: none)
+};
+
+// Row r (whole warp): its session and what it needs.
+template <typename T>
+__device__ SlotInfo resolve_row(const RowArgs& A, long long r) {
+  SlotInfo s{-1, 0, true, -1};
+  const SessIO& io = A.io;
+  const long long R_T = io.total + io.B;
+  if (r >= R_T + io.total) return s;
+  const bool is_target = r < R_T;
+  const int32_t b = find_session(io.m_offsets, io.B, is_target ? r : r - R_T, is_target);
+  const RowCtx x = row_ctx(A, r, b, sizeof(T) == 2);
+  s.row_id = r;
+  s.b = b;
+  s.skip = x.skip;
+  s.xt = x.has_x ? io.tokens[x.tok_idx] : -1;
+  return s;
 }
 
 // --------------------------------------------------------------------------------------
@@ -778,9 +862,9 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
   extern __shared__ __align__(128) unsigned char ring[];  // kStages * kChunk bytes
   __shared__ RowShared sh;
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
-  const long long nrows = A.total + A.B + A.total;
-
+  const long long nrows = 2 * A.io.total + A.io.B;
   pdl_launch_dependents();  // the session kernel may start its prologue now
+
   if (t == 0) {
     for (int s = 0; s < kStages; ++s) { mbar_init(&sh.full[s], 1); mbar_init(&sh.empty[s], kConsWarps); }
     sh.abort = 0;
@@ -789,32 +873,31 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
   __syncthreads();
 
   if (w == kProducerWarp) {
-    // ---------------- producer: stream the CTA's rows into the ring ----------------
+    // ---------------- producer: claim rows, stream them into the ring ----------------
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    // session of a row (warp-cooperative search); the next row's is looked up while the
-    // current row streams, so its latency is hidden behind the copies in flight
-    auto session_of = [&](long long r) -> int {
-      const bool is_target = r < A.total + A.B;
-      return find_session(A.m_offsets, A.B, is_target ? r : r - (A.total + A.B), is_target);
+    auto fetch = [&]() -> long long {
+      unsigned long long r = 0;
+      if (l == 0) r = atomicAdd(&A.hdr->next_slot, 1ull);
+      return (long long)__shfl_sync(0xFFFFFFFFu, r, 0);
     };
-    long long r = blockIdx.x;
-    int b = (r < nrows) ? session_of(r) : 0;
-    for (; r < nrows && ok; r += gridDim.x) {
-      const RowCtx x = row_ctx(A, r, b, sizeof(T) == 2);
-      const long long rn = r + gridDim.x;
-      int bn = 0;
-      if (x.skip) {
-        if (l == 0) write_skipped(A, r);
-        b = (rn < nrows) ? session_of(rn) : 0;
+    long long rcur = fetch();
+    SlotInfo cur = resolve_row<T>(A, rcur);
+    while (ok && rcur < nrows) {
+      if (cur.skip) {
+        if (l == 0) write_skipped(A, cur.row_id);
+        rcur = fetch();
+        cur = resolve_row<T>(A, rcur);
         continue;
       }
-      const T* row = row_ptr<T>(A, r);
-      const RowLayout L = row_layout(row, A.V);
+      const T* row = row_ptr<T>(A, cur.row_id);
+      const RowLayout L = row_layout(row, A.io.V);
       const long long vbytes = L.nvec * 16;
       const int nch = (int)max(1ll, (vbytes + kChunk - 1) / kChunk);
       const char* src = reinterpret_cast<const char*>(row + L.head);
+      long long rnext = nrows;
+      SlotInfo nxt{-1, 0, true, -1};
       for (int c = 0; c < nch && ok; ++c) {
         if (l == 0) {
           if (!mbar_wait(&sh.empty[stage], phase ^ 1u, kWaitPolls) || sh.abort) {
@@ -822,16 +905,20 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
           } else {
             const long long off = (long long)c * kChunk;
             const uint32_t bytes = (uint32_t)max(0ll, min((long long)kChunk, vbytes - off));
-            if (c == 0) { sh.plan[stage].row_id = r; sh.plan[stage].b = b; sh.plan[stage].nchunks = nch; }
+            if (c == 0) sh.plan[stage] = RowPlan{cur.row_id, cur.b, nch, cur.xt};
             mbar_arrive_expect_tx(&sh.full[stage], bytes);
             if (bytes > 0) bulk_copy_g2s(ring + (size_t)stage * kChunk, src + off, bytes, &sh.full[stage]);
           }
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
-        if (c == 0 && rn < nrows) bn = session_of(rn);  // overlaps the copies in flight
+        if (c == 0 && ok) {  // the next row, while the copies are in flight
+          rnext = fetch();
+          nxt = resolve_row<T>(A, rnext);
+        }
       }
-      b = bn;
+      rcur = rnext;
+      cur = nxt;
     }
     if (l == 0) {
       if (ok && mbar_wait(&sh.empty[stage], phase ^ 1u, kWaitPolls) && !sh.abort) {
@@ -839,7 +926,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
         mbar_arrive_expect_tx(&sh.full[stage], 0);
       } else {
         sh.abort = 1;
-        atomicOr(A.error, 1u);
+        atomicOr(&A.hdr->error, 1u);
         // let copies already issued land before the CTA can exit (bounded)
         for (int s = 0; s < kStages; ++s) {
           (void)mbar_wait(&sh.full[s], 0, 1 << 12);
@@ -848,39 +935,44 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       }
     }
     return;
-  }
-
-  // ---------------- consumers ----------------
-  const Group g{kCons, kConsBar};
-  int stage = 0;
-  uint32_t phase = 0;
-  ThreadAcc acc;
-  acc.reset();
-  while (true) {
-    if (!mbar_wait(&sh.full[stage], phase, kWaitPolls)) sh.abort = 1;
-    g.sync();
-    if (sh.abort) break;
-    const RowPlan plan = sh.plan[stage];
-    if (plan.row_id < 0) break;
-    const RowCtx x = row_ctx(A, plan.row_id, plan.b, sizeof(T) == 2);
-    const T* row = row_ptr<T>(A, plan.row_id);
-    const RowLayout L = row_layout(row, A.V);
-    if (x.window) {  // fresh window for this row (ordered before use by the barrier below)
-      for (int i = t; i < kWindowBins; i += kCons) sh.hist[i] = 0u;
-      if (t == 0) sh.win_over = 0;
-    }
-    bool fail = false;
-    for (int c = 0; c < plan.nchunks; ++c) {
-      if (c > 0 && !mbar_wait(&sh.full[stage], phase, kWaitPolls)) { fail = true; break; }
-      const long long off = (long long)c * kChunk;
-      const int nv = (int)(max(0ll, min((long long)kChunk, L.nvec * 16 - off)) / 16);
-      const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)stage * kChunk);
-      const long long id0 = L.head + (off / 16) * Elem<T>::kPerVec;
-      acc_stage_mode<T>(x.mode, acc, sv, nv, id0, x.c);
-      if (x.window) {
-        if (c == 0) {
-          // anchor: the maximum of the first stage; the window keeps every token within
-          // dz nats of it, and room for values up to 2047 bf16 steps above its bottom
+  } else {
+    // ---------------- consumers ----------------
+    const Group g{kCons, kConsBar};
+    int stage = 0;
+    uint32_t phase = 0;
+    ThreadAcc acc;
+    acc.reset();
+    while (true) {
+      if (!mbar_wait(&sh.full[stage], phase, kWaitPolls)) sh.abort = 1;
+      g.sync();
+      if (sh.abort) break;
+      const RowPlan plan = sh.plan[stage];
+      if (plan.row_id < 0) break;
+      const RowCtx x = row_ctx(A, plan.row_id, plan.b, sizeof(T) == 2);
+      const T* row = row_ptr<T>(A, plan.row_id);
+      const RowLayout L = row_layout(row, A.io.V);
+      if (x.window)  // fresh window for this row (ordered before use by the anchor's barriers)
+        for (int i = t; i < kWindowBins; i += kCons) sh.hist[i] = 0u;
+      // the draft token's logit, loaded while the first stage is reduced
+      const bool want_x = x.has_x && plan.xt >= 0 && (int64_t)plan.xt < A.io.V;
+      uint32_t xbits = 0u;
+      if (t == 0 && want_x) xbits = load_bits(row, plan.xt);
+      bool fail = false;
+      for (int c = 0; c < plan.nchunks; ++c) {
+        if (c > 0 && !mbar_wait(&sh.full[stage], phase, kWaitPolls)) { fail = true; break; }
+        const long long off = (long long)c * kChunk;
+        const int nv = (int)(max(0ll, min((long long)kChunk, L.nvec * 16 - off)) / 16);
+        const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)stage * kChunk);
+        const long long id0 = L.head + (off / 16) * Elem<T>::kPerVec;
+        if (!x.window || (c > 0 && !sh.win_on)) {
+          acc_stage_mode<T, 0>(x.mode, acc, sh, sv, nv, id0, x.c);
+        } else if (c > 0) {
+          if (sh.win_pos) acc_stage_mode<T, 1>(x.mode, acc, sh, sv, nv, id0, x.c);
+          else acc_stage_mode<T, 2>(x.mode, acc, sh, sv, nv, id0, x.c);
+        } else {
+          acc_stage_mode<T, 0>(x.mode, acc, sh, sv, nv, id0, x.c);
+          // anchor: the maximum of the first stage; the window keeps every token within dz
+          // nats of it, and room for values up to 2047 bf16 steps above its bottom
           const float wm = warp_reduce(acc.fm, [](float a, float b) { return fmax_nan(a, b); });
           if (l == 0) sh.w_fm[w] = wm;
           g.sync();
@@ -893,32 +985,38 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
             if (sh.win_on) {
               uint32_t lo16 = order_key(__float_as_uint((float)lo)) >> 16;
               lo16 = lo16 > (kKeyNegInf >> 16) ? lo16 - 1 : (kKeyNegInf >> 16);
+              const uint32_t top16 = min(lo16 + (uint32_t)(kWindowBins - 1), 0xFF7Fu);
               sh.win_lo = key_value(lo16 << 16);
-              sh.win_top16 = min(lo16 + (uint32_t)(kWindowBins - 1), 0xFF7Fu);
+              sh.win_top16 = top16;
+              sh.win_nb = (int)(top16 - lo16 + 1);
+              sh.win_pos = lo16 > 0x8000u ? 1 : 0;
+              sh.win_hih = (int)top16 - 0x8000;
             }
           }
           g.sync();
+          if (sh.win_on) window_stage<T>(sh, sv, nv);
         }
-        if (sh.win_on) window_stage<T>(sh, sv, nv);
+        __syncwarp();
+        if (l == 0) mbar_arrive(&sh.empty[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
-      __syncwarp();
-      if (l == 0) mbar_arrive(&sh.empty[stage]);
-      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      if (t == 0) sh.xbits = xbits;  // read by finish_row after its first barrier
+      if (fail) sh.abort = 1;
+      g.sync();
+      if (sh.abort) break;
+      finish_row<T>(A, sh, x, plan, acc);
+      acc.reset();
     }
-    if (fail) sh.abort = 1;
-    g.sync();
-    if (sh.abort) break;
-    finish_row<T>(A, sh, x, plan.row_id, acc);
-    acc.reset();
+    if (t == 0 && sh.abort) atomicOr(&A.hdr->error, 1u);
   }
-  if (t == 0 && sh.abort) atomicOr(A.error, 1u);
+
 }
 
 template __global__ void row_stats_kernel<float>(RowArgs);
 template __global__ void row_stats_kernel<__nv_bfloat16>(RowArgs);
 
 int launch_row_stats(const RowArgs& a, int dtype, cudaStream_t stream) {
-  const long long rows = a.total + a.B + a.total;
+  const long long rows = a.io.total + a.io.B + a.io.total;
   if (rows <= 0) return 0;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
