@@ -40,6 +40,7 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 KERNEL_SOURCES = ["speculative_decoding_verification_sdcp_gb300/csrc/sdcp_rows.cu",
+                  "speculative_decoding_verification_sdcp_gb300/csrc/sdcp_session.cuh",
                   "speculative_decoding_verification_sdcp_gb300/csrc/sdcp_device.cuh"]
 
 
@@ -53,6 +54,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sessions", type=int, default=None,
+                    help="keep only the first N sessions of the workload (small cases for ncu)")
     return ap.parse_args()
 
 
@@ -231,7 +234,7 @@ def run_ours(args, dist: Dist):
     dev = torch.device("cuda", dist.local)
     torch.cuda.set_device(dev)
     w = synth.WORKLOADS[args.workload]
-    batch = synth.make_batch(w, device=dev)
+    batch = synth.make_batch(w, device=dev, max_sessions=args.sessions)
     ver = binding.Verifier(batch.V, batch.B, batch.total_drafts, dev)
     ab = synth.algorithmic_bytes(batch)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -341,7 +344,8 @@ def run_ours(args, dist: Dist):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_max_ranks, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "description": w.note, "B": batch.B, "V": batch.V,
+            "config": {"workload": w.name if args.sessions is None else "%s (first %d sessions)" % (w.name, batch.B),
+                       "description": w.note, "B": batch.B, "V": batch.V,
                        "total_drafts": batch.total_drafts, "logits_dtype": "bf16" if batch.dtype_code == 1 else "f32",
                        "l2": "flushed between timed steps (256 MiB write)",
                        "parallelism": "sessions sharded by GPU (dp%d)" % dist.world},
@@ -374,7 +378,7 @@ def run_reference(args, dist: Dist):
     oracle.build()
     w = synth.WORKLOADS[args.workload]
     dev = "cuda:%d" % dist.local if torch.cuda.is_available() else "cpu"
-    batch = synth.make_batch(w, device=dev)
+    batch = synth.make_batch(w, device=dev, max_sessions=args.sessions)
     cores = len(os.sched_getaffinity(0))
     per = min(batch.B, cores)
     B = batch.B

@@ -103,6 +103,18 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   return y;
 }
 
+// The sampling profile's temperature as the kernels apply it (Section 4.1: logits / T with
+// T = temperature_milli / 1000), in fp32 so no per-row step needs the slow fp64 pipe:
+// c = log2(e) * 1000 / T, so that exp((l - m) / T) = 2^((l - m) c), and the inverse scale
+// T / 1000 that turns nats into logit units.  Every kernel uses these two, so the row
+// statistics and the draws agree bit for bit.
+__device__ __forceinline__ float profile_c(uint32_t temperature_milli) {
+  return __fdiv_rn(1442.6950408889634f, (float)temperature_milli);
+}
+__device__ __forceinline__ float profile_inv_scale(uint32_t temperature_milli) {
+  return (float)temperature_milli * 0.001f;
+}
+
 // ---------------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): per round the pair of 32x32->64
 // products with multipliers 0xD2511F53 (of word 0) and 0xCD9E8D57 (of word 2) is mixed

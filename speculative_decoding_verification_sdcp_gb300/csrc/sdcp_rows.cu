@@ -263,8 +263,7 @@ struct RowCtx {
   bool skip, is_target, has_x, one_hot, topk, topp, need_keys, need_sum, need_max, window;
   int b;
   long long tok_idx;
-  double scale_d;
-  float c;
+  float c, inv_scale;  // log2(e) 1000/T; T/1000
   sdcp_session_params P;
   int mode;
 };
@@ -296,8 +295,8 @@ __device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, in
   }
   const uint32_t tm = x.P.temperature_milli;
   x.one_hot = (tm == 0u);
-  x.scale_d = x.one_hot ? 0.0 : 1000.0 / (double)tm;
-  x.c = (float)(x.scale_d * 1.4426950408889634);  // log2(e) * 1000/T
+  x.c = x.one_hot ? 0.f : profile_c(tm);
+  x.inv_scale = profile_inv_scale(tm);
   x.topk = !x.one_hot && want_profile && x.P.top_k != 0u && (int64_t)x.P.top_k < A.io.V;
   x.topp = !x.one_hot && want_profile && x.P.top_p_milli < 1000u;
   x.need_keys = want_argmax || x.one_hot;  // the argmax is needed
@@ -484,7 +483,7 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
   }
   int dcut = dk, ncut = tk;
   if (x.topp) {
-    const float target = (float)((double)x.P.top_p_milli / 1000.0 * (double)s_base);
+    const float target = (float)x.P.top_p_milli * 0.001f * s_base;
     int cd = -1, cn = 0;
     float cb = 0.f;
     long long ccb = 0;
@@ -498,7 +497,7 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
       const float md = (float)avail * e;
       const float nxt = cum + md;
       if (md > 0.f && nxt >= target) {
-        long long n = (long long)ceil(((double)target - (double)cum) / (double)e);
+        long long n = (long long)ceilf(__fdiv_rn(target - cum, e));
         if (n < 1) n = 1;
         if (n > avail) n = avail;
         cd = d; cn = (int)n; cb = cum; ccb = cc;
@@ -563,9 +562,9 @@ __device__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, c
   if ((int64_t)nb > (int64_t)kmax16 - (int64_t)(kKeyNegInf >> 16) + 1)
     nb = (int)((int64_t)kmax16 - (int64_t)(kKeyNegInf >> 16) + 1);
   if (dz > 0.f) {
-    const double lo = (double)lmax - (double)dz / x.scale_d;
-    if (lo > -3.0e38 && lo < (double)lmax) {
-      uint32_t klo16 = order_key(__float_as_uint((float)lo)) >> 16;
+    const float lo = lmax - dz * x.inv_scale;
+    if (lo > -3.0e38f && lo < lmax) {
+      uint32_t klo16 = order_key(__float_as_uint(lo)) >> 16;
       klo16 = klo16 > 0 ? klo16 - 1 : 0;
       if (klo16 < kmax16 && (int64_t)(kmax16 - klo16 + 1) < nb) nb = (int)(kmax16 - klo16 + 1);
     }
@@ -636,7 +635,7 @@ __device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, 
   const float s1 = mass_ge(0u);
   float skept = s1;
   if (x.topp) {
-    const float target = (float)((double)x.P.top_p_milli / 1000.0 * (double)s1);
+    const float target = (float)x.P.top_p_milli * 0.001f * s1;
     uint32_t lo = 0u, hi = kmax_f;
     while (lo < hi) {
       const uint32_t mid = lo + (uint32_t)(((uint64_t)hi - lo + 1) / 2);
@@ -652,7 +651,7 @@ __device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, 
     const long long cnt_above = group_sum_ll(g, ca, sh.lscr);
     const long long avail = group_sum_ll(g, av, sh.lscr);
     const float e1 = ex2((key_value(kp) - lmax) * x.c);
-    long long n = (long long)ceil(((double)target - (double)above) / (double)e1);
+    long long n = (long long)ceilf(__fdiv_rn(target - above, e1));
     if (n < 1) n = 1;
     if (n > avail) n = avail;
     kcut = kp;
@@ -822,7 +821,7 @@ __device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, con
       if (!(flags & kRowHasX)) q.lp_x = __int_as_float(0x7FC00000);
       else if (!(flags & SDCP_ROW_X_KEPT)) q.lp_x = -INFINITY;
       else if (x.one_hot) q.lp_x = 0.f;
-      else q.lp_x = (float)((double)st.dlx * x.scale_d - log((double)st.s));
+      else q.lp_x = (float)((double)st.dlx * (1000.0 / (double)x.P.temperature_milli) - log((double)st.s));
       A.pub[row_id] = q;
     }
   }
@@ -980,10 +979,10 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
             float m0 = -INFINITY;
             for (int i = 0; i < kConsWarps; ++i) m0 = fmax_nan(m0, sh.w_fm[i]);
             const float dz = x.topp ? 11.f : 8.f;
-            const double lo = (double)m0 - (double)dz / x.scale_d;
-            sh.win_on = (m0 == m0 && m0 > -INFINITY && m0 < INFINITY && lo > -3.0e38) ? 1 : 0;
+            const float lo = m0 - dz * x.inv_scale;
+            sh.win_on = (m0 == m0 && m0 > -INFINITY && m0 < INFINITY && lo > -3.0e38f) ? 1 : 0;
             if (sh.win_on) {
-              uint32_t lo16 = order_key(__float_as_uint((float)lo)) >> 16;
+              uint32_t lo16 = order_key(__float_as_uint(lo)) >> 16;
               lo16 = lo16 > (kKeyNegInf >> 16) ? lo16 - 1 : (kKeyNegInf >> 16);
               const uint32_t top16 = min(lo16 + (uint32_t)(kWindowBins - 1), 0xFF7Fu);
               sh.win_lo = key_value(lo16 << 16);

@@ -1,8 +1,9 @@
 // sdcp_sessions.cu - phase 2 of the acceptance step (SDCP draft
 // draft-li-mlc-inference-acceleration-00, Section 6.3 "Preconditions of the rule" and
-// Section 6.4 Rules 1 and 2): one CTA per session runs the completion of sdcp_session.cuh
-// on the row statistics phase 1 left in the workspace.  Launched as a programmatic
-// dependent of the row kernel, it waits for the row statistics before reading them.
+// Section 6.4 Rules 1 and 2): one thread-block cluster per session runs the completion of
+// sdcp_session.cuh on the row statistics phase 1 left in the workspace.  Launched as a
+// programmatic dependent of the row kernel, it waits for the row statistics before
+// reading them.
 #include "sdcp_session.cuh"
 
 namespace sdcp {
@@ -10,26 +11,45 @@ namespace sdcp {
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) session_kernel(SessIO A) {
   __shared__ SessSmem sm;
+  cg::cluster_group cluster = cg::this_cluster();
   const Group g{kThreads, 1};
   pdl_wait_primary();  // the row statistics and the error word are complete from here on
-  complete_session<T>(A, g, sm, (int32_t)blockIdx.x);
+  complete_session<T>(A, cluster, g, sm, (int32_t)(blockIdx.x / cluster.num_blocks()));
 }
 
 template __global__ void session_kernel<float>(SessIO);
 template __global__ void session_kernel<__nv_bfloat16>(SessIO);
 
+// CTAs per session: enough clusters x CTAs to give every SM two CTAs when the batch is
+// small, never slices under 32 segments (8192 ids) of a row; 1 .. 8.
+static int session_cluster(int64_t V, int32_t B) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  int64_t c = (2 * (int64_t)sms + B - 1) / (B > 0 ? B : 1);
+  const int64_t by_size = (V + 8191) / 8192;
+  if (c > by_size) c = by_size;
+  return (int)(c < 1 ? 1 : (c > 8 ? 8 : c));
+}
+
 int launch_sessions(const SessIO& a, int dtype, bool pdl, cudaStream_t stream) {
   if (a.B <= 0) return 0;
+  const int C = session_cluster(a.V, a.B);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.B, 1, 1);
+  cfg.gridDim = dim3((unsigned)((int64_t)a.B * C), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = pdl ? 2 : 1;
   cudaError_t e;
   if (dtype == SDCP_BF16)
     e = cudaLaunchKernelEx(&cfg, session_kernel<__nv_bfloat16>, a);
