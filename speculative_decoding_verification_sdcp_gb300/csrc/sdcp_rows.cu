@@ -363,7 +363,7 @@ __device__ __forceinline__ void visit_row(const T* __restrict__ row, const RowLa
 template <typename T, typename F>
 __device__ __forceinline__ void scan_row(const T* __restrict__ row, const RowLayout& L, int64_t V, F f) {
   constexpr int E = Elem<T>::kPerVec;
-  constexpr int U = 8;
+  constexpr int U = 4;
   const int t = threadIdx.x;
   for (int64_t j = t; j < L.head; j += kCons) {
     uint32_t b[E];
@@ -553,7 +553,7 @@ __device__ __forceinline__ bool get_thresholds(const RowShared& sh, Thresholds& 
 // Window histogram of the tokens within dz nats below the row maximum (dz = 0: the 2048
 // values below it), from a pass over the row in L2, then the selection (group).
 template <typename T>
-__device__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
+__device__ __noinline__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
                                   const RowCtx& x, int64_t V, float lmax, float s_all, float dz,
                                   Thresholds& out) {
   const int t = threadIdx.x;
@@ -596,7 +596,7 @@ __device__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, c
 
 // Generic search: bisection over the order-key space with group-wide reductions.
 template <typename T>
-__device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
+__device__ __noinline__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
                                    const RowCtx& x, int64_t V, float lmax, uint32_t kmax_f,
                                    Thresholds& out) {
   auto count_ge = [&](uint32_t kk) -> long long {
@@ -678,7 +678,7 @@ __device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, 
 
 // Tokens with order key `key` and an id below xt (group; second read of the row, from L2).
 template <typename T>
-__device__ long long count_key_before(const Group& g, RowShared& sh, const T* row, int64_t xt, uint32_t key) {
+__device__ __noinline__ long long count_key_before(const Group& g, RowShared& sh, const T* row, int64_t xt, uint32_t key) {
   const bool al = ((uintptr_t)row & 15u) == 0;
   long long c = 0;
 #pragma unroll 4

@@ -22,10 +22,31 @@ namespace sdcp {
 
 constexpr int kSegIds = 32 * kEpt;  // ids per segment: 8 per lane
 constexpr int kSegCap = 2048;       // segment-group sums held in shared memory
+constexpr int kTieCap = 64;         // tokens on a cut value held per warp (single-pass draw)
+constexpr int kTieStages = 64;      // stages whose cut-value counts are kept (single-pass draw)
+constexpr int kDrawHalf = 16384;    // bytes of p (and of q) per stage of the streamed draw
+constexpr int kDrawStages = 2;      // stages of the streamed draw's ring
+constexpr long long kDrawPolls = 1ll << 22;
 
-// Shared memory of one CTA of a session's cluster.
+// A token whose keptness depends on its rank among the tokens of a cut value (p's or q's).
+struct TieEntry {
+  int id;
+  float P, Q;  // its p and q weights were it kept
+  int code;    // bit 0: on p's cut value; bit 1: on q's cut value; bits 8..: stage
+  int lp, lq;  // its index among p's (q's) cut-value tokens of its stage and warp
+};
+
+// Shared memory of one CTA of a session's cluster (the streamed draw's ring is dynamic).
 struct SessSmem {
+  uint64_t full[kDrawStages], empty[kDrawStages];
   float seg[kSegCap];  // per segment group of the CTA's slice: weight sums or tie counts
+  TieEntry ties[kWarps][kTieCap];  // per warp, in id order within each stage
+  int tie_n[kWarps];
+  int tsc_p[kTieStages][kWarps], tsc_q[kTieStages][kWarps];  // cut-value tokens per stage, warp
+  int overflow;
+  long long cta_np, cta_nq;  // cut-value tokens of the slice (read by the cluster)
+  int cta_ovf;
+  int tie_p_cand, tie_q_cand;  // id bounds found in this slice (read by the cluster)
   float fscr[2 * 32 + 4];
   long long lscr[2 * 32 + 4];
   float cta_sum;       // the slice's total weight (read by the cluster)
@@ -34,6 +55,7 @@ struct SessSmem {
   long long owner_pre, owner_carry;
   long long result;    // a tie id found by this CTA (read by the cluster)
   int st, a, draw;
+  uint32_t ring_uses;  // stages of the draw ring used so far (slot and barrier parity)
 };
 
 // Verdict of a session: status, accepted count, and whether Rule 2 still draws a token.
@@ -203,6 +225,22 @@ __device__ __forceinline__ void unpack_raw8(const Raw8<T>& r, uint32_t (&b)[kEpt
   }
 }
 
+// f(bits of p, bits of q, e) for the 8 elements of one lane piece, in id order, straight from
+// the loaded words (no per-element arrays: they would not fit the register budget).
+template <typename T, typename F>
+__device__ __forceinline__ void for_each8(const Raw8<T>& rp, const Raw8<T>& rq, F f) {
+  if constexpr (sizeof(T) == 2) {
+    f(rp.v[0].x << 16, rq.v[0].x << 16, 0); f(rp.v[0].x & 0xFFFF0000u, rq.v[0].x & 0xFFFF0000u, 1);
+    f(rp.v[0].y << 16, rq.v[0].y << 16, 2); f(rp.v[0].y & 0xFFFF0000u, rq.v[0].y & 0xFFFF0000u, 3);
+    f(rp.v[0].z << 16, rq.v[0].z << 16, 4); f(rp.v[0].z & 0xFFFF0000u, rq.v[0].z & 0xFFFF0000u, 5);
+    f(rp.v[0].w << 16, rq.v[0].w << 16, 6); f(rp.v[0].w & 0xFFFF0000u, rq.v[0].w & 0xFFFF0000u, 7);
+  } else {
+    f(rp.v[0].x, rq.v[0].x, 0); f(rp.v[0].y, rq.v[0].y, 1); f(rp.v[0].z, rq.v[0].z, 2); f(rp.v[0].w, rq.v[0].w, 3);
+    f(rp.v[Raw8<T>::W - 1].x, rq.v[Raw8<T>::W - 1].x, 4); f(rp.v[Raw8<T>::W - 1].y, rq.v[Raw8<T>::W - 1].y, 5);
+    f(rp.v[Raw8<T>::W - 1].z, rq.v[Raw8<T>::W - 1].z, 6); f(rp.v[Raw8<T>::W - 1].w, rq.v[Raw8<T>::W - 1].w, 7);
+  }
+}
+
 // The segments of one CTA's slice of a row (ids are int: V <= SDCP_MAX_VOCAB): segments
 // [s0, s1) of 256 ids, grouped G at a time into ngrp <= kSegCap groups; warp w owns groups
 // [ngrp w / 8, ngrp (w + 1) / 8).
@@ -250,8 +288,7 @@ __device__ void draw_pass(const SegSlice& sl, SessSmem& sm, const T* prow, const
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int a, b;
   sl.warp_range(w, kWarps, a, b);
-  // segments whose loads are in flight together (fewer with the cut test: registers)
-  constexpr int U = ((sizeof(T) == 2) ? 8 : 4) / (FILT ? 2 : 1);
+  constexpr int U = (sizeof(T) == 2) ? 4 : 2;  // segments whose loads are in flight together
   float gacc = 0.f;
   for (int k = a; k < b; k += U) {
     Raw8<T> rp[U], rq[U];
@@ -267,8 +304,13 @@ __device__ void draw_pass(const SegSlice& sl, SessSmem& sm, const T* prow, const
     for (int u = 0; u < U; ++u) {
       const int kk = k + u;
       if (kk < b) {
-        float wv[kEpt];
-        const float ls = piece_weights<T, FILT>(rp[u], rq[u], residual, pr, qr, kk * kSegIds + lane * kEpt, wv);
+        const int j0 = kk * kSegIds + lane * kEpt;
+        float ls = 0.f;
+        for_each8<T>(rp[u], rq[u], [&](uint32_t bp, uint32_t bq, int e) {
+          float x = draw_weight<FILT>(pr, bp, j0 + e);
+          if (residual) x = fmaxf(x - draw_weight<FILT>(qr, bq, j0 + e), 0.f);
+          ls += x;
+        });
         gacc += warp_reduce(ls, [](float x, float y) { return x + y; });
         if ((kk - sl.s0 + 1) % sl.G == 0 || kk + 1 == sl.s1) {
           if (lane == 0) sm.seg[(kk - sl.s0) / sl.G] = gacc;
@@ -282,7 +324,7 @@ __device__ void draw_pass(const SegSlice& sl, SessSmem& sm, const T* prow, const
 // One warp walks segments [k0, k1) from cumulative weight `carry`: the smallest id whose
 // cumulative weight exceeds target, else (rounding) the largest id with positive weight seen.
 template <typename T, bool FILT>
-__device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p, bool al_q, int V,
+__device__ __noinline__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p, bool al_q, int V,
                          const DrawRow& pr, const DrawRow& qr, int k0, int k1, float carry,
                          float target, bool last_only) {
   const int lane = threadIdx.x & 31;
@@ -322,19 +364,21 @@ __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p,
   return lastpos;
 }
 
-// The draw over the cluster: the token goes to out (by the one CTA that finds it).  Returns
-// W, the total weight (the same in every CTA).
+
+// ---------------------------------------------------------------------------------
+// Locating the token: the slices' totals through distributed shared memory, the CTA
+// whose slice holds u * W scans its segment sums, one warp walks the segment.
+// ---------------------------------------------------------------------------------
+
+// Returns W (the same in every CTA), or NaN when some CTA of the cluster flagged its pass
+// as unusable (sm.overflow).  Tie ids come from the CTAs' candidates when `ties`.
 template <typename T, bool FILT>
-__device__ __noinline__ float draw_token(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
-                                         const T* prow, const T* qrow, bool residual, bool al_p,
-                                         bool al_q, int V, const DrawRow& pr, const DrawRow& qr,
-                                         double u1, int32_t* out) {
-  const int t = threadIdx.x, w = t >> 5;
+__device__ __noinline__ float locate_and_walk(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+                                              const SegSlice& sl, const T* prow, const T* qrow, bool residual,
+                                              bool al_p, bool al_q, int V, DrawRow pr, DrawRow qr,
+                                              bool pp, bool qp, double u1, int32_t* out) {
+  const int t = threadIdx.x, w = t >> 5, lane = t & 31;
   const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
-  const SegSlice sl(V, C, rank);
-  draw_pass<T, FILT>(sl, sm, prow, qrow, residual, al_p, al_q, V, pr, qr);
-  g.sync();
-  // this slice's groups in id order: thread t owns groups [t gpt, t gpt + gpt)
   const int gpt = (sl.ngrp + g.nthreads - 1) / g.nthreads;
   float loc = 0.f;
   for (int i = 0; i < gpt; ++i) {
@@ -343,17 +387,18 @@ __device__ __noinline__ float draw_token(cg::cluster_group& cluster, const Group
   }
   float Wc;
   const float pre = group_excl_scan(g, loc, sm.fscr, &Wc);
-  if (t == 0) sm.cta_sum = Wc;
+  if (t == 0) { sm.cta_sum = Wc; sm.cta_ovf = sm.overflow; }
   cluster.sync();
-  // the slices in rank order
-  float W = 0.f, base = 0.f;
-  int owner = -1, lastr = -1;
+  float W = 0.f;
+  int owner = -1, lastr = -1, tp_id = INT_MAX, tq_id = INT_MAX, bad = 0;
   float obase = 0.f;
   for (unsigned r = 0; r < C; ++r) {
     const float sr = *cluster.map_shared_rank(&sm.cta_sum, r);
-    if (r == rank) base = W;
-    W += sr;
     if (sr > 0.f) lastr = (int)r;
+    W += sr;
+    tp_id = min(tp_id, *cluster.map_shared_rank(&sm.tie_p_cand, r));
+    tq_id = min(tq_id, *cluster.map_shared_rank(&sm.tie_q_cand, r));
+    bad |= *cluster.map_shared_rank(&sm.cta_ovf, r);
   }
   const float target = (float)(u1 * (double)W);
   {
@@ -365,10 +410,12 @@ __device__ __noinline__ float draw_token(cg::cluster_group& cluster, const Group
     }
   }
   cluster.sync();  // every CTA has read the slice totals
+  if (bad) return __int_as_float(0x7FC00000);
   if (!(W > 0.f)) return W;
   const bool mine = (owner == (int)rank) || (owner < 0 && lastr == (int)rank);
   if (!mine) return W;
-  // this CTA's slice holds the token: its segment group, then the walk
+  pr.tie = pp ? tp_id : INT_MAX;
+  qr.tie = qp ? tq_id : INT_MAX;
   long long cand = LLONG_MAX, lastg = -1;
   float cbase = 0.f;
   if (owner >= 0) {
@@ -398,9 +445,334 @@ __device__ __noinline__ float draw_token(cg::cluster_group& cluster, const Group
       tok = draw_walk<T, FILT>(prow, qrow, residual, al_p, al_q, V, pr, qr, sl.grp_lo((int)lg),
                                sl.grp_hi((int)lg), 0.f, 0.f, true);
     }
-    if ((t & 31) == 0) *out = tok;
+    if (lane == 0) *out = tok;
   }
   return W;
+}
+
+// ---------------------------------------------------------------------------------
+// Tokens on a cut value (the single-pass draws): left out of the segment sums during the
+// pass and held, with both weights, in a per-warp list in id order within each stage.
+// ---------------------------------------------------------------------------------
+
+// Clears the per-call state of the cut-value tokens (group).
+__device__ __forceinline__ void ties_reset(const Group& g, SessSmem& sm) {
+  for (int i = threadIdx.x; i < kTieStages * kWarps; i += g.nthreads) {
+    (&sm.tsc_p[0][0])[i] = 0;
+    (&sm.tsc_q[0][0])[i] = 0;
+  }
+  if (threadIdx.x == 0) { sm.overflow = 0; sm.tie_p_cand = INT_MAX; sm.tie_q_cand = INT_MAX; }
+  if (threadIdx.x < kWarps) sm.tie_n[threadIdx.x] = 0;
+}
+
+// Appends the lane's cut-value tokens of one piece (amb; cp / cq: on p's / q's cut value),
+// lanes in order, to the warp's list, and counts them for stage st.  Whole warp, only when
+// some lane has such a token (rare: called out of line).
+template <typename T>
+__device__ __noinline__ void tie_append(SessSmem& sm, const Raw8<T>& rp, const Raw8<T>& rq, bool residual,
+                                        const DrawRow& pr, const DrawRow& qr, int j0, uint32_t amb,
+                                        uint32_t cp, uint32_t cq, int st, int& nt, bool& ovf) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = __popc(amb), cnp = __popc(cp), cnq = __popc(cq);
+  int incl = c, ip = cnp, iq = cnq;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a1 = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    const int a2 = __shfl_up_sync(0xFFFFFFFFu, ip, o);
+    const int a3 = __shfl_up_sync(0xFFFFFFFFu, iq, o);
+    if (lane >= o) { incl += a1; ip += a2; iq += a3; }
+  }
+  const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  const int tp = __shfl_sync(0xFFFFFFFFu, ip, 31), tq = __shfl_sync(0xFFFFFFFFu, iq, 31);
+  if (ovf || st >= kTieStages || nt + total > kTieCap) { ovf = true; return; }
+  const int bp = sm.tsc_p[st][w], bq = sm.tsc_q[st][w];
+  __syncwarp();
+  int pos = nt + incl - c, lp = bp + ip - cnp, lq = bq + iq - cnq;
+  for_each8<T>(rp, rq, [&](uint32_t xp, uint32_t xq, int e) {
+    if ((amb >> e) & 1u) {
+      const float vp = __uint_as_float(xp), vq = __uint_as_float(xq);
+      const float P = (vp >= pr.thr) ? ex2(fmaf(vp, pr.c, -pr.bias)) : 0.f;
+      const float Q = (residual && vq >= qr.thr) ? ex2(fmaf(vq, qr.c, -qr.bias)) : 0.f;
+      const int ep = (cp >> e) & 1u, eq = (cq >> e) & 1u;
+      sm.ties[w][pos] = TieEntry{j0 + e, P, Q, ep | (eq << 1) | (st << 8), lp, lq};
+      ++pos;
+      lp += ep;
+      lq += eq;
+    }
+  });
+  if (lane == 0) { sm.tsc_p[st][w] = bp + tp; sm.tsc_q[st][w] = bq + tq; }
+  nt += total;
+  __syncwarp();
+}
+
+// After the pass (group, every CTA of the cluster): the rank of a cut-value token is its
+// index among the cluster's tokens of that cut value in id order (slices in rank order,
+// then stages, then warps, then list order); the first thr_n are kept.  Their weights
+// join the segment sums (each warp adds its own, in id order) and the id bound of the kept
+// ones goes to sm.tie_*_cand.  Returns false when a list overflowed anywhere (uniform).
+static __device__ __noinline__ bool resolve_ties(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+                                          const SegSlice& sl, int nstages, bool residual, int np_cut,
+                                          int nq_cut) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
+  if (t == 0) {  // exclusive prefix per (stage, warp) within the slice
+    int ap = 0, aq = 0;
+    for (int s = 0; s < nstages && s < kTieStages; ++s)
+      for (int i = 0; i < kWarps; ++i) {
+        const int cp = sm.tsc_p[s][i], cq = sm.tsc_q[s][i];
+        sm.tsc_p[s][i] = ap; sm.tsc_q[s][i] = aq;
+        ap += cp; aq += cq;
+      }
+    sm.cta_np = ap; sm.cta_nq = aq; sm.cta_ovf = sm.overflow;
+  }
+  cluster.sync();
+  long long P0 = 0, Q0 = 0;
+  int ovf_any = 0;
+  for (unsigned r = 0; r < C; ++r) {
+    if (r < rank) { P0 += *cluster.map_shared_rank(&sm.cta_np, r); Q0 += *cluster.map_shared_rank(&sm.cta_nq, r); }
+    ovf_any |= *cluster.map_shared_rank(&sm.cta_ovf, r);
+  }
+  cluster.sync();  // every CTA has read the counts
+  if (ovf_any) return false;
+  TieEntry* L = sm.ties[w];
+  const int nt = sm.tie_n[w];
+  for (int i = lane; i < nt; i += 32) {
+    const TieEntry en = L[i];
+    const int st = en.code >> 8, isp = en.code & 1, isq = (en.code >> 1) & 1;
+    const long long rp = P0 + sm.tsc_p[st][w] + en.lp, rq = Q0 + sm.tsc_q[st][w] + en.lq;
+    const bool kp = !isp || rp < np_cut, kq = !isq || rq < nq_cut;
+    if (isp && rp == (long long)np_cut - 1) sm.tie_p_cand = en.id;
+    if (isq && rq == (long long)nq_cut - 1) sm.tie_q_cand = en.id;
+    const float P = kp ? en.P : 0.f, Q = kq ? en.Q : 0.f;
+    L[i].P = residual ? fmaxf(P - Q, 0.f) : P;  // the token's weight
+  }
+  __syncwarp();
+  if (lane == 0)  // into the segment sums, in id order
+    for (int i = 0; i < nt; ++i) sm.seg[(L[i].id / kSegIds - sl.s0) / sl.G] += L[i].P;
+  g.sync();
+  return true;
+}
+
+// ---------------------------------------------------------------------------------
+// The draw from global memory (any row alignment, any slice length).
+// ---------------------------------------------------------------------------------
+
+// Without cut-value tokens to rank: every token's weight is known during the pass.
+template <typename T, bool FILT>
+__device__ __noinline__ float draw_token(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+                                         const T* prow, const T* qrow, bool residual, bool al_p,
+                                         bool al_q, int V, const DrawRow& pr, const DrawRow& qr,
+                                         double u1, int32_t* out) {
+  const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
+  const SegSlice sl(V, C, rank);
+  if (threadIdx.x == 0) { sm.overflow = 0; sm.tie_p_cand = INT_MAX; sm.tie_q_cand = INT_MAX; }
+  draw_pass<T, FILT>(sl, sm, prow, qrow, residual, al_p, al_q, V, pr, qr);
+  g.sync();
+  return locate_and_walk<T, FILT>(cluster, g, sm, sl, prow, qrow, residual, al_p, al_q, V, pr, qr,
+                                  false, false, u1, out);
+}
+
+// A cut inside a value (p's, q's or both), in one pass; NaN when a list overflowed.
+template <typename T>
+__device__ __noinline__ float draw_token_ties(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+                                              const T* prow, const T* qrow, bool residual, bool al_p,
+                                              bool al_q, int V, const DrawRow& pr, const DrawRow& qr,
+                                              int np_cut, int nq_cut, double u1, int32_t* out) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
+  const SegSlice sl(V, C, rank);
+  const bool pp = np_cut != INT_MAX, qp = residual && nq_cut != INT_MAX;
+  ties_reset(g, sm);
+  g.sync();
+  {
+    int a, b;
+    sl.warp_range(w, kWarps, a, b);
+    constexpr int U = 2;
+    float gacc = 0.f;
+    int nt = 0;
+    bool ovf = false;
+    for (int k = a; k < b; k += U) {
+      Raw8<T> rp[U], rq[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j0 = (k + u) * kSegIds + lane * kEpt;
+        if (k + u < b) {
+          load_raw8<T>(prow, al_p, V, j0, rp[u]);
+          if (residual) load_raw8<T>(qrow, al_q, V, j0, rq[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int kk = k + u;
+        if (kk >= b) continue;
+        const int j0 = kk * kSegIds + lane * kEpt;
+        uint32_t amb = 0u, cp = 0u, cq = 0u;
+        float ls = 0.f;
+        for_each8<T>(rp[u], rq[u], [&](uint32_t bp, uint32_t bq, int e) {
+          const float vp = __uint_as_float(bp), vq = __uint_as_float(bq);
+          const bool tp = pp && vp == pr.thr, tq = qp && vq == qr.thr;
+          float x = (vp >= pr.thr) ? ex2(fmaf(vp, pr.c, -pr.bias)) : 0.f;
+          if (residual) x = fmaxf(x - ((vq >= qr.thr) ? ex2(fmaf(vq, qr.c, -qr.bias)) : 0.f), 0.f);
+          const bool am = tp || tq;  // on a cut value: weighed after the pass
+          amb |= (am ? 1u : 0u) << e;
+          cp |= (tp ? 1u : 0u) << e;
+          cq |= (tq ? 1u : 0u) << e;
+          ls += am ? 0.f : x;
+        });
+        gacc += warp_reduce(ls, [](float x, float y) { return x + y; });
+        if ((kk - sl.s0 + 1) % sl.G == 0 || kk + 1 == sl.s1) {
+          if (lane == 0) sm.seg[(kk - sl.s0) / sl.G] = gacc;
+          gacc = 0.f;
+        }
+        if (__any_sync(0xFFFFFFFFu, amb != 0u))
+          tie_append<T>(sm, rp[u], rq[u], residual, pr, qr, j0, amb, cp, cq, 0, nt, ovf);
+      }
+    }
+    if (lane == 0) {
+      sm.tie_n[w] = nt;
+      if (ovf) sm.overflow = 1;
+    }
+  }
+  g.sync();
+  if (!resolve_ties(cluster, g, sm, sl, 1, residual, np_cut, nq_cut)) return __int_as_float(0x7FC00000);
+  return locate_and_walk<T, true>(cluster, g, sm, sl, prow, qrow, residual, al_p, al_q, V, pr, qr, pp, qp,
+                                  u1, out);
+}
+
+// ---------------------------------------------------------------------------------
+// The streamed draw: thread 0 copies the CTA's slice of p (and q) into a two-stage ring
+// of shared memory with bulk copies (TMA) that complete on mbarriers, 16 KB of each row
+// per stage; each warp reduces its segments of a stage from shared memory and hands the
+// stage back.  Needs 16-byte aligned rows, V a multiple of 8, one segment per group (a
+// slice of at most 2048 segments) and, with cut-value tokens, at most kTieStages stages.
+// Returns W, or NaN when it could not decide (a list overflowed, a wait gave up): the
+// caller then draws from global memory.
+// ---------------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ bool stream_ok(int V, unsigned C, unsigned rank, bool al, bool ties) {
+  const SegSlice sl(V, C, rank);
+  constexpr int S = kDrawHalf / (int)sizeof(T);
+  const int n = min(sl.s1 * kSegIds, V) - sl.s0 * kSegIds;
+  return al && (V % 8) == 0 && sl.G == 1 && (!ties || (n + S - 1) / S <= kTieStages);
+}
+
+template <typename T, bool FILT, bool TIES>
+__device__ __noinline__ float draw_stream(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+                                          unsigned char* ring, const T* prow, const T* qrow, bool residual,
+                                          int V, const DrawRow& pr, const DrawRow& qr, int np_cut,
+                                          int nq_cut, double u1, int32_t* out) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
+  const SegSlice sl(V, C, rank);
+  constexpr int S = kDrawHalf / (int)sizeof(T);  // ids per stage
+  constexpr int SPW = S / kSegIds / kWarps;       // segments of a warp per stage
+  static_assert(SPW >= 1 && SPW * kWarps * kSegIds == S, "stage layout");
+  const int lo = sl.s0 * kSegIds, hi = min(sl.s1 * kSegIds, V);
+  const int nst = (hi > lo) ? (hi - lo + S - 1) / S : 0;
+  const bool pp = TIES && np_cut != INT_MAX, qp = TIES && residual && nq_cut != INT_MAX;
+  const uint32_t use0 = sm.ring_uses;
+  (void)pp; (void)qp;
+  if (TIES) ties_reset(g, sm);
+  else if (t == 0) { sm.overflow = 0; sm.tie_p_cand = INT_MAX; sm.tie_q_cand = INT_MAX; }
+  g.sync();  // every thread has read ring_uses
+  bool fail = false;
+  auto issue = [&](int s) {  // thread 0: stage s of the slice into its slot
+    const uint32_t u = use0 + (uint32_t)s;
+    const int slot = (int)(u % kDrawStages);
+    if (u >= kDrawStages && !mbar_wait(&sm.empty[slot], ((u / kDrawStages) - 1) & 1u, kDrawPolls)) {
+      fail = true;
+      return;
+    }
+    const int n = min(S, hi - (lo + s * S));
+    const uint32_t bytes = (uint32_t)n * sizeof(T);
+    unsigned char* dst = ring + (size_t)slot * 2 * kDrawHalf;
+    mbar_arrive_expect_tx(&sm.full[slot], residual ? 2 * bytes : bytes);
+    bulk_copy_g2s(dst, prow + lo + s * S, bytes, &sm.full[slot]);
+    if (residual) bulk_copy_g2s(dst + kDrawHalf, qrow + lo + s * S, bytes, &sm.full[slot]);
+  };
+  if (t == 0)
+    for (int s = 0; s < nst && s < kDrawStages; ++s) issue(s);
+  int nt = 0;
+  bool ovf = false;
+  for (int s = 0; s < nst; ++s) {
+    const uint32_t u = use0 + (uint32_t)s;
+    const int slot = (int)(u % kDrawStages);
+    if (!mbar_wait(&sm.full[slot], (u / kDrawStages) & 1u, kDrawPolls)) fail = true;
+    const unsigned char* src = ring + (size_t)slot * 2 * kDrawHalf;
+    const int stage_lo = lo + s * S;
+#pragma unroll 1
+    for (int i = 0; i < SPW; ++i) {
+      const int sis = w * SPW + i;  // segment in the stage
+      const int seg_lo = stage_lo + sis * kSegIds;
+      if (seg_lo >= hi) continue;  // past the slice (warp-uniform)
+      const int j0 = seg_lo + lane * kEpt;
+      Raw8<T> rp, rq;
+      const uint4* pv = reinterpret_cast<const uint4*>(src + (size_t)(sis * kSegIds + lane * kEpt) * sizeof(T));
+#pragma unroll
+      for (int q = 0; q < Raw8<T>::W; ++q) rp.v[q] = pv[q];
+      if (residual) {
+        const uint4* qv = reinterpret_cast<const uint4*>(src + kDrawHalf + (size_t)(sis * kSegIds + lane * kEpt) * sizeof(T));
+#pragma unroll
+        for (int q = 0; q < Raw8<T>::W; ++q) rq.v[q] = qv[q];
+      }
+      if (j0 + kEpt > hi) {  // the row's last segment: ids past V read as -inf
+        uint32_t* a = reinterpret_cast<uint32_t*>(rp.v);
+        uint32_t* bq = reinterpret_cast<uint32_t*>(rq.v);
+#pragma unroll
+        for (int e = 0; e < kEpt; ++e) {
+          if (j0 + e >= hi) {
+            if (sizeof(T) == 2) {
+              a[e >> 1] = (e & 1) ? ((a[e >> 1] & 0x0000FFFFu) | 0xFF800000u) : ((a[e >> 1] & 0xFFFF0000u) | 0xFF80u);
+              bq[e >> 1] = (e & 1) ? ((bq[e >> 1] & 0x0000FFFFu) | 0xFF800000u) : ((bq[e >> 1] & 0xFFFF0000u) | 0xFF80u);
+            } else {
+              a[e] = 0xFF800000u;
+              bq[e] = 0xFF800000u;
+            }
+          }
+        }
+      }
+      uint32_t amb = 0u, cp = 0u, cq = 0u;
+      float ls = 0.f;
+      for_each8<T>(rp, rq, [&](uint32_t bp, uint32_t bqq, int e) {
+        if (!TIES) {
+          float x = draw_weight<FILT>(pr, bp, j0 + e);
+          if (residual) x = fmaxf(x - draw_weight<FILT>(qr, bqq, j0 + e), 0.f);
+          ls += x;
+        } else {
+          const float vp = __uint_as_float(bp), vq = __uint_as_float(bqq);
+          const bool tp = pp && vp == pr.thr, tq = qp && vq == qr.thr;
+          float x = (vp >= pr.thr) ? ex2(fmaf(vp, pr.c, -pr.bias)) : 0.f;
+          if (residual) x = fmaxf(x - ((vq >= qr.thr) ? ex2(fmaf(vq, qr.c, -qr.bias)) : 0.f), 0.f);
+          const bool am = tp || tq;
+          amb |= (am ? 1u : 0u) << e;
+          cp |= (tp ? 1u : 0u) << e;
+          cq |= (tq ? 1u : 0u) << e;
+          ls += am ? 0.f : x;
+        }
+      });
+      const float ssum = warp_reduce(ls, [](float x, float y) { return x + y; });
+      if (lane == 0) sm.seg[(seg_lo - lo) / kSegIds] = ssum;
+      if (TIES && __any_sync(0xFFFFFFFFu, amb != 0u))
+        tie_append<T>(sm, rp, rq, residual, pr, qr, j0, amb, cp, cq, s, nt, ovf);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    if (t == 0 && s + kDrawStages < nst) issue(s + kDrawStages);
+  }
+  if (TIES && lane == 0) sm.tie_n[w] = nt;
+  if (lane == 0 && (ovf || fail)) sm.overflow = 1;
+  if (t == 0 && fail) {  // a wait gave up: let the copies already issued land first (bounded)
+    for (int s = max(0, nst - kDrawStages); s < nst; ++s) {
+      const uint32_t u = use0 + (uint32_t)s;
+      (void)mbar_wait(&sm.full[u % kDrawStages], (u / kDrawStages) & 1u, 1 << 14);
+    }
+  }
+  if (t == 0) sm.ring_uses = use0 + (uint32_t)nst;
+  g.sync();
+  if (TIES && !resolve_ties(cluster, g, sm, sl, nst, residual, np_cut, nq_cut)) return __int_as_float(0x7FC00000);
+  const bool al_p = ((uintptr_t)prow & 15u) == 0, al_q = ((uintptr_t)qrow & 15u) == 0;
+  return locate_and_walk<T, FILT || TIES>(cluster, g, sm, sl, prow, qrow, residual, al_p, al_q, V, pr, qr,
+                                          pp, qp, u1, out);
 }
 
 // Id of the n-th token (1-based, id order) with value `val` over the cluster (every CTA
@@ -413,7 +785,7 @@ __device__ __noinline__ int cut_tie_id(cg::cluster_group& cluster, const Group& 
   const SegSlice sl(V, C, rank);
   int a, b;
   sl.warp_range(w, kWarps, a, b);
-  constexpr int U = (sizeof(T) == 2) ? 16 : 8;
+  constexpr int U = (sizeof(T) == 2) ? 4 : 2;
   int gacc = 0;
   for (int k = a; k < b; k += U) {
     Raw8<T> r[U];
@@ -510,7 +882,7 @@ __device__ __noinline__ int cut_tie_id(cg::cluster_group& cluster, const Group& 
 // Rule 2's draw for session b whose first rejection is a (a == M: the bonus from p_M).
 template <typename T>
 __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const Group& g, SessSmem& sm,
-                             int32_t b, int a) {
+                             unsigned char* ring, int32_t b, int a) {
   const sdcp_session_params P = A.params[b];
   const int64_t off0 = A.m_offsets[b], off1 = A.m_offsets[b + 1];
   const int64_t M = off1 - off0;
@@ -522,6 +894,7 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
   const RowStat sq = (a < M) ? load_stat(A.stats + R_T + off0 + a) : sp;
   const float c = profile_c(P.temperature_milli);
   const bool al_p = ((uintptr_t)trow & 15u) == 0, al_q = ((uintptr_t)drow & 15u) == 0;
+  const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
   bool residual = (a < M);
   const bool filt_p = sp.thr_key != 0u || sp.thr_n != INT_MAX;
   const bool filt_q = residual && (sq.thr_key != 0u || sq.thr_n != INT_MAX);
@@ -531,18 +904,40 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
   qr.bias = fmaf(sq.lmax, c, log2f(sq.s));
   pr.thr = filt_p ? key_value(sp.thr_key) : -INFINITY;
   qr.thr = filt_q ? key_value(sq.thr_key) : -INFINITY;
-  // id bound of the kept tokens at the cut value, where the cut falls inside a value
-  pr.tie = (sp.thr_n == INT_MAX) ? INT_MAX : cut_tie_id<T>(cluster, g, sm, trow, al_p, V, pr.thr, sp.thr_n);
-  qr.tie = (!residual || sq.thr_n == INT_MAX) ? INT_MAX
-                                              : cut_tie_id<T>(cluster, g, sm, drow, al_q, V, qr.thr, sq.thr_n);
+  pr.tie = INT_MAX;
+  qr.tie = INT_MAX;
   const double u1 = verifier_uniform(P, (uint32_t)a, 1u);
-  const bool filt = filt_p || filt_q;
   int32_t* out = A.out_tokens + off0 + b + a;
   for (int attempt = 0; attempt < 2; ++attempt) {
-    const float W = filt ? draw_token<T, true>(cluster, g, sm, trow, drow, residual, al_p, al_q, V, pr, qr, u1, out)
-                         : draw_token<T, false>(cluster, g, sm, trow, drow, residual, al_p, al_q, V, pr, qr, u1, out);
-    if (!(W > 0.f) && residual) { residual = false; continue; }  // residual mass lost to rounding: use p
-    if (!(W > 0.f) && cluster.block_rank() == 0 && threadIdx.x == 0) *out = -1;
+    const bool filt = filt_p || (residual && filt_q);
+    const int np_cut = sp.thr_n, nq_cut = residual ? sq.thr_n : INT_MAX;
+    const bool ties = np_cut != INT_MAX || nq_cut != INT_MAX;
+    float W = __int_as_float(0x7FC00000);
+    // first choice: stream the slice through shared memory (the same decision in every CTA)
+    bool ok_all = true;
+    for (unsigned r = 0; r < C; ++r) ok_all = ok_all && stream_ok<T>(V, C, r, al_p && (al_q || !residual), ties);
+    if (attempt == 0 && ok_all) {
+      if (ties) W = draw_stream<T, true, true>(cluster, g, sm, ring, trow, drow, residual, V, pr, qr, np_cut, nq_cut, u1, out);
+      else if (filt) W = draw_stream<T, true, false>(cluster, g, sm, ring, trow, drow, residual, V, pr, qr, np_cut, nq_cut, u1, out);
+      else W = draw_stream<T, false, false>(cluster, g, sm, ring, trow, drow, residual, V, pr, qr, np_cut, nq_cut, u1, out);
+    }
+    if (W != W && ties) {  // from global memory: one pass with the lists, else tie ids first
+      W = draw_token_ties<T>(cluster, g, sm, trow, drow, residual, al_p, al_q, V, pr, qr, np_cut, nq_cut, u1, out);
+      if (W != W) {
+        pr.tie = (np_cut == INT_MAX) ? INT_MAX : cut_tie_id<T>(cluster, g, sm, trow, al_p, V, pr.thr, np_cut);
+        qr.tie = (nq_cut == INT_MAX) ? INT_MAX : cut_tie_id<T>(cluster, g, sm, drow, al_q, V, qr.thr, nq_cut);
+        W = draw_token<T, true>(cluster, g, sm, trow, drow, residual, al_p, al_q, V, pr, qr, u1, out);
+      }
+    } else if (W != W) {
+      W = filt ? draw_token<T, true>(cluster, g, sm, trow, drow, residual, al_p, al_q, V, pr, qr, u1, out)
+               : draw_token<T, false>(cluster, g, sm, trow, drow, residual, al_p, al_q, V, pr, qr, u1, out);
+    }
+    if (!(W > 0.f) && residual) {  // residual mass lost to rounding: use p
+      residual = false;
+      pr.tie = INT_MAX;
+      continue;
+    }
+    if (!(W > 0.f) && rank == 0 && threadIdx.x == 0) *out = -1;
     break;
   }
 }
@@ -550,7 +945,7 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
 // Verdict in every CTA of the cluster (rank 0 writes it), then the draw if Rule 2 needs one.
 template <typename T>
 __device__ __noinline__ void complete_session(const SessIO& A, cg::cluster_group& cluster, const Group& g,
-                                              SessSmem& sm, int32_t b) {
+                                              SessSmem& sm, unsigned char* ring, int32_t b) {
   if ((threadIdx.x >> 5) == 0) {
     const Verdict v = session_verdict(A, b, cluster.block_rank() == 0);
     if ((threadIdx.x & 31) == 0) { sm.st = v.st; sm.a = v.a; sm.draw = v.draw ? 1 : 0; }
@@ -558,7 +953,7 @@ __device__ __noinline__ void complete_session(const SessIO& A, cg::cluster_group
   g.sync();
   const int a = sm.a, draw = sm.draw;
   g.sync();
-  if (draw) session_draw<T>(A, cluster, g, sm, b, a);  // the same in every CTA of the cluster
+  if (draw) session_draw<T>(A, cluster, g, sm, ring, b, a);  // the same in every CTA of the cluster
 }
 
 }  // namespace sdcp

@@ -8,27 +8,37 @@
 
 namespace sdcp {
 
+constexpr size_t kRingBytes = (size_t)kDrawStages * 2 * kDrawHalf;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) session_kernel(SessIO A) {
+  extern __shared__ __align__(128) unsigned char ring[];  // the streamed draw's stages
   __shared__ SessSmem sm;
   cg::cluster_group cluster = cg::this_cluster();
   const Group g{kThreads, 1};
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDrawStages; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], kWarps); }
+    sm.ring_uses = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
   pdl_wait_primary();  // the row statistics and the error word are complete from here on
-  complete_session<T>(A, cluster, g, sm, (int32_t)(blockIdx.x / cluster.num_blocks()));
+  complete_session<T>(A, cluster, g, sm, ring, (int32_t)(blockIdx.x / cluster.num_blocks()));
 }
 
 template __global__ void session_kernel<float>(SessIO);
 template __global__ void session_kernel<__nv_bfloat16>(SessIO);
 
-// CTAs per session: enough clusters x CTAs to give every SM two CTAs when the batch is
-// small, never slices under 32 segments (8192 ids) of a row; 1 .. 8.
+// CTAs per session: as many as fit two CTAs per SM over the whole batch (a draw is a
+// latency-bound chain, so small batches gain from splitting it), never slices under 32
+// segments (8192 ids) of a row; 1 .. 8.
 static int session_cluster(int64_t V, int32_t B) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 148;
-  int64_t c = (2 * (int64_t)sms + B - 1) / (B > 0 ? B : 1);
-  const int64_t by_size = (V + 8191) / 8192;
+  int64_t c = (2 * (int64_t)sms) / (B > 0 ? B : 1);
+  const int64_t by_size = V / 8192;
   if (c > by_size) c = by_size;
   return (int)(c < 1 ? 1 : (c > 8 ? 8 : c));
 }
@@ -39,7 +49,7 @@ int launch_sessions(const SessIO& a, int dtype, bool pdl, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((int64_t)a.B * C), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kRingBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -50,7 +60,10 @@ int launch_sessions(const SessIO& a, int dtype, bool pdl, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  cudaError_t e;
+  const void* fn = (dtype == SDCP_BF16) ? (const void*)session_kernel<__nv_bfloat16>
+                                        : (const void*)session_kernel<float>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingBytes);
+  if (e != cudaSuccess) return (int)e;
   if (dtype == SDCP_BF16)
     e = cudaLaunchKernelEx(&cfg, session_kernel<__nv_bfloat16>, a);
   else

@@ -93,6 +93,27 @@ def test_ties_and_tie_overflow():
     _parity(batch)
 
 
+@pytest.mark.parametrize("top_k,top_p", [(50, 1000), (0, 900), (200, 950)])
+def test_cut_value_ties_in_both_rows(top_k, top_p):
+    """Logits on a 0.5 grid: the cut of p and the cut of q both fall inside a value shared
+    by tens of tokens, so the residual draw must rank the tokens of both cut values (the
+    single-pass draw); the drafter samples its tokens from the quantised q."""
+    B, V, M = 10, 32000, 4
+    w = synth.custom_workload(B=B, V=V, dtype=synth.BF16, m=M, rules="spec", temperature_milli=800,
+                              top_k=top_k, top_p_milli=top_p, gen_seed=21)
+    batch = synth.make_batch(w, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    t = torch.round(torch.randn(batch.target.shape, generator=g, device=DEV) * 6.0) / 2.0
+    d = torch.round((t[: batch.total_drafts] + torch.randn(batch.draft.shape, generator=g, device=DEV))
+                    * 2.0) / 2.0
+    batch.target.copy_(t.to(torch.bfloat16))
+    batch.draft.copy_(d.to(torch.bfloat16))
+    batch.draft_tokens.copy_(synth.drafter_sample(batch.draft, 800, top_k, top_p, g))
+    got, counts = _parity(batch)
+    assert (got["status"] == 0).all(), got["status"]
+    assert counts["exact"] >= B - 2, counts
+
+
 def test_flat_distribution_window_fallback():
     """Logits within +-0.05 straddle zero: the nucleus spans many binades below the max
     and the window cannot hold it, so the generic search decides."""
