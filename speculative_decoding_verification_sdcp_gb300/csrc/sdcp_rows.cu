@@ -553,7 +553,7 @@ __device__ __forceinline__ bool get_thresholds(const RowShared& sh, Thresholds& 
 // Window histogram of the tokens within dz nats below the row maximum (dz = 0: the 2048
 // values below it), from a pass over the row in L2, then the selection (group).
 template <typename T>
-__device__ __noinline__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
+__device__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
                                   const RowCtx& x, int64_t V, float lmax, float s_all, float dz,
                                   Thresholds& out) {
   const int t = threadIdx.x;
@@ -596,7 +596,7 @@ __device__ __noinline__ bool window_thresholds(const Group& g, RowShared& sh, co
 
 // Generic search: bisection over the order-key space with group-wide reductions.
 template <typename T>
-__device__ __noinline__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
+__device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, const RowLayout& L,
                                    const RowCtx& x, int64_t V, float lmax, uint32_t kmax_f,
                                    Thresholds& out) {
   auto count_ge = [&](uint32_t kk) -> long long {
@@ -678,7 +678,7 @@ __device__ __noinline__ void generic_thresholds(const Group& g, RowShared& sh, c
 
 // Tokens with order key `key` and an id below xt (group; second read of the row, from L2).
 template <typename T>
-__device__ __noinline__ long long count_key_before(const Group& g, RowShared& sh, const T* row, int64_t xt, uint32_t key) {
+__device__ long long count_key_before(const Group& g, RowShared& sh, const T* row, int64_t xt, uint32_t key) {
   const bool al = ((uintptr_t)row & 15u) == 0;
   long long c = 0;
 #pragma unroll 4
@@ -911,7 +911,10 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
         }
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
-        if (c == 0 && ok) {  // the next row, while the copies are in flight
+        // the next row once this row's last stage is issued (its copies and the stages
+        // queued before it cover the lookup); claiming earlier would let a busy CTA hold a
+        // row that an idle one could take, which lengthens the tail
+        if (c == nch - 1 && ok) {
           rnext = fetch();
           nxt = resolve_row<T>(A, rnext);
         }

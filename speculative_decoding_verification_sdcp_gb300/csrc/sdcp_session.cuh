@@ -76,7 +76,7 @@ __device__ __forceinline__ RowStat load_stat(const RowStat* p) {
 // Verdict (one full warp; every lane returns the same value).  Writes status, accepted,
 // n_out and every output slot except the drawn token.
 // ---------------------------------------------------------------------------------
-static __device__ __noinline__ Verdict session_verdict(const SessIO& A, int32_t b, bool write) {
+static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write) {
   const int lane = threadIdx.x & 31;
   const sdcp_session_params P = A.params[b];
   const int64_t off0 = A.m_offsets[b], off1 = A.m_offsets[b + 1];
@@ -324,7 +324,7 @@ __device__ void draw_pass(const SegSlice& sl, SessSmem& sm, const T* prow, const
 // One warp walks segments [k0, k1) from cumulative weight `carry`: the smallest id whose
 // cumulative weight exceeds target, else (rounding) the largest id with positive weight seen.
 template <typename T, bool FILT>
-__device__ __noinline__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p, bool al_q, int V,
+__device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p, bool al_q, int V,
                          const DrawRow& pr, const DrawRow& qr, int k0, int k1, float carry,
                          float target, bool last_only) {
   const int lane = threadIdx.x & 31;
@@ -373,7 +373,7 @@ __device__ __noinline__ int draw_walk(const T* prow, const T* qrow, bool residua
 // Returns W (the same in every CTA), or NaN when some CTA of the cluster flagged its pass
 // as unusable (sm.overflow).  Tie ids come from the CTAs' candidates when `ties`.
 template <typename T, bool FILT>
-__device__ __noinline__ float locate_and_walk(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+__device__ float locate_and_walk(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                               const SegSlice& sl, const T* prow, const T* qrow, bool residual,
                                               bool al_p, bool al_q, int V, DrawRow pr, DrawRow qr,
                                               bool pp, bool qp, double u1, int32_t* out) {
@@ -467,9 +467,9 @@ __device__ __forceinline__ void ties_reset(const Group& g, SessSmem& sm) {
 
 // Appends the lane's cut-value tokens of one piece (amb; cp / cq: on p's / q's cut value),
 // lanes in order, to the warp's list, and counts them for stage st.  Whole warp, only when
-// some lane has such a token (rare: called out of line).
+// some lane has such a token.
 template <typename T>
-__device__ __noinline__ void tie_append(SessSmem& sm, const Raw8<T>& rp, const Raw8<T>& rq, bool residual,
+__device__ void tie_append(SessSmem& sm, const Raw8<T>& rp, const Raw8<T>& rq, bool residual,
                                         const DrawRow& pr, const DrawRow& qr, int j0, uint32_t amb,
                                         uint32_t cp, uint32_t cq, int st, int& nt, bool& ovf) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -510,7 +510,7 @@ __device__ __noinline__ void tie_append(SessSmem& sm, const Raw8<T>& rp, const R
 // then stages, then warps, then list order); the first thr_n are kept.  Their weights
 // join the segment sums (each warp adds its own, in id order) and the id bound of the kept
 // ones goes to sm.tie_*_cand.  Returns false when a list overflowed anywhere (uniform).
-static __device__ __noinline__ bool resolve_ties(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+static __device__ bool resolve_ties(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                           const SegSlice& sl, int nstages, bool residual, int np_cut,
                                           int nq_cut) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -559,7 +559,7 @@ static __device__ __noinline__ bool resolve_ties(cg::cluster_group& cluster, con
 
 // Without cut-value tokens to rank: every token's weight is known during the pass.
 template <typename T, bool FILT>
-__device__ __noinline__ float draw_token(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+__device__ float draw_token(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                          const T* prow, const T* qrow, bool residual, bool al_p,
                                          bool al_q, int V, const DrawRow& pr, const DrawRow& qr,
                                          double u1, int32_t* out) {
@@ -574,7 +574,7 @@ __device__ __noinline__ float draw_token(cg::cluster_group& cluster, const Group
 
 // A cut inside a value (p's, q's or both), in one pass; NaN when a list overflowed.
 template <typename T>
-__device__ __noinline__ float draw_token_ties(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+__device__ float draw_token_ties(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                               const T* prow, const T* qrow, bool residual, bool al_p,
                                               bool al_q, int V, const DrawRow& pr, const DrawRow& qr,
                                               int np_cut, int nq_cut, double u1, int32_t* out) {
@@ -657,7 +657,7 @@ __device__ __forceinline__ bool stream_ok(int V, unsigned C, unsigned rank, bool
 }
 
 template <typename T, bool FILT, bool TIES>
-__device__ __noinline__ float draw_stream(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+__device__ float draw_stream(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                           unsigned char* ring, const T* prow, const T* qrow, bool residual,
                                           int V, const DrawRow& pr, const DrawRow& qr, int np_cut,
                                           int nq_cut, double u1, int32_t* out) {
@@ -778,7 +778,7 @@ __device__ __noinline__ float draw_stream(cg::cluster_group& cluster, const Grou
 // Id of the n-th token (1-based, id order) with value `val` over the cluster (every CTA
 // gets it); INT_MAX if none.
 template <typename T>
-__device__ __noinline__ int cut_tie_id(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+__device__ int cut_tie_id(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                        const T* row, bool al, int V, float val, int n) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
@@ -944,7 +944,7 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
 
 // Verdict in every CTA of the cluster (rank 0 writes it), then the draw if Rule 2 needs one.
 template <typename T>
-__device__ __noinline__ void complete_session(const SessIO& A, cg::cluster_group& cluster, const Group& g,
+__device__ void complete_session(const SessIO& A, cg::cluster_group& cluster, const Group& g,
                                               SessSmem& sm, unsigned char* ring, int32_t b) {
   if ((threadIdx.x >> 5) == 0) {
     const Verdict v = session_verdict(A, b, cluster.block_rank() == 0);
