@@ -52,16 +52,11 @@ struct RowShared {
   uint64_t empty[kStages];
   RowPlan plan[kStages];
   volatile int abort;
-  // per-warp partials
-  float w_fm[32], w_s[32];
+  // per-warp partials (w_m0: the first stage's maxima, for the window's anchor)
+  float w_fm[32], w_s[32], w_m0[32];
   long long w_amax[32];
   float fscr[2 * 32 + 4];
   long long lscr[2 * 32 + 4];
-  // window of the row being streamed: bin d counts the tokens whose bf16 value key is
-  // win_top16 - d (d < win_nb); positive windows index bins by bit pattern, d = win_hih - h
-  float win_lo;
-  uint32_t win_top16;
-  int win_nb, win_on, win_pos, win_hih;
   uint32_t xbits;  // the draft token's logit bits
   // the merged row and its cut (warp 0 -> group)
   float r_lmax, r_s, r_skept;
@@ -143,11 +138,12 @@ __device__ __forceinline__ float acc_vector(ThreadAcc& a, const uint4& q, long l
 }
 
 // --------------------------------------------------------------------------------------
-// Window histogram.  Every element of a bf16 row with a filter updates the bin of its value
-// under a predicate.  Positive windows (bottom above +0): with h the bf16 bit pattern as a
-// signed 16-bit number, value order is h order and d = win_hih - h is in [0, nb) exactly
-// for the window's values (negative values have h < 0, values above the top d < 0).
-// Other windows go through the order key: d = win_top16 - key16.
+// Window histogram.  Bin d counts the tokens whose bf16 value key is top16 - d (d < nb).
+// Every element of a bf16 row with a filter updates the bin of its value under a predicate.
+// Positive windows (bottom above +0): with h the bf16 bit pattern as a signed 16-bit number,
+// value order is h order and d = (top16 - 0x8000) - h is in [0, nb) exactly for the
+// window's values (negative values have h < 0, values above the top give d < 0).  Other
+// windows go through the order key: d = top16 - key16.
 // --------------------------------------------------------------------------------------
 template <bool POS>
 __device__ __forceinline__ void win_word(uint32_t* hist, uint32_t wd, uint32_t top, uint32_t nb) {
@@ -172,9 +168,9 @@ __device__ __forceinline__ void win_vector(uint32_t* hist, const uint4& q, uint3
   }
 }
 // One element (bits of a bf16 value in the upper half) of the row's unaligned ends.
-__device__ __forceinline__ void win_scalar(RowShared& sh, uint32_t bits) {
-  const uint32_t d = sh.win_top16 - (order_key(bits) >> 16);
-  if (d < (uint32_t)sh.win_nb) atomicAdd(sh.hist + d, 1u);
+__device__ __forceinline__ void win_scalar(RowShared& sh, uint32_t bits, uint32_t top16, uint32_t nb) {
+  const uint32_t d = top16 - (order_key(bits) >> 16);
+  if (d < nb) atomicAdd(sh.hist + d, 1u);
 }
 
 // Vectors [0, nv) of one ring stage (nv <= kVecPerThread * kCons); vector v is element
@@ -183,11 +179,9 @@ __device__ __forceinline__ void win_scalar(RowShared& sh, uint32_t bits) {
 // changes no statistic and no bin.
 template <typename T, bool ARGMAX, bool SUM, int WIN>
 __device__ __forceinline__ void acc_stage(ThreadAcc& a, RowShared& sh, const uint4* sv, int nv,
-                                          long long id0, float c) {
+                                          long long id0, float c, uint32_t top, uint32_t nb) {
   constexpr int E = Elem<T>::kPerVec;
   const int t = threadIdx.x;
-  const uint32_t top = (WIN == 1) ? (uint32_t)sh.win_hih : sh.win_top16;
-  const uint32_t nb = (uint32_t)sh.win_nb;
   const uint32_t ninf = (sizeof(T) == 2) ? 0xFF80FF80u : 0xFF800000u;
   const uint4 pad = make_uint4(ninf, ninf, ninf, ninf);
 #pragma unroll 1
@@ -210,11 +204,9 @@ __device__ __forceinline__ void acc_stage(ThreadAcc& a, RowShared& sh, const uin
 
 // The window over a stage that was reduced before the window was placed (the first).
 template <typename T>
-__device__ __forceinline__ void window_stage(RowShared& sh, const uint4* sv, int nv) {
+__device__ __forceinline__ void window_stage(RowShared& sh, const uint4* sv, int nv, bool pos, uint32_t top,
+                                             uint32_t nb) {
   const int t = threadIdx.x;
-  const bool pos = sh.win_pos != 0;
-  const uint32_t top = pos ? (uint32_t)sh.win_hih : sh.win_top16;
-  const uint32_t nb = (uint32_t)sh.win_nb;
 #pragma unroll 4
   for (int i = 0; i < kVecPerThread; ++i) {
     const int v = t + i * kCons;
@@ -237,12 +229,12 @@ enum RowMode { kModeMax = 0, kModeArgmax = 1, kModeSum = 2, kModeArgmaxSum = 3 }
 
 template <typename T, int WIN>
 __device__ __forceinline__ void acc_stage_mode(int mode, ThreadAcc& a, RowShared& sh, const uint4* sv, int nv,
-                                               long long id0, float c) {
+                                               long long id0, float c, uint32_t top = 0u, uint32_t nb = 0u) {
   switch (mode) {
-    case kModeMax: acc_stage<T, false, false, WIN>(a, sh, sv, nv, id0, c); break;
-    case kModeArgmax: acc_stage<T, true, false, WIN>(a, sh, sv, nv, id0, c); break;
-    case kModeSum: acc_stage<T, false, true, WIN>(a, sh, sv, nv, id0, c); break;
-    default: acc_stage<T, true, true, WIN>(a, sh, sv, nv, id0, c); break;
+    case kModeMax: acc_stage<T, false, false, WIN>(a, sh, sv, nv, id0, c, top, nb); break;
+    case kModeArgmax: acc_stage<T, true, false, WIN>(a, sh, sv, nv, id0, c, top, nb); break;
+    case kModeSum: acc_stage<T, false, true, WIN>(a, sh, sv, nv, id0, c, top, nb); break;
+    default: acc_stage<T, true, true, WIN>(a, sh, sv, nv, id0, c, top, nb); break;
   }
 }
 template <typename T>
@@ -694,11 +686,12 @@ __device__ long long count_key_before(const Group& g, RowShared& sh, const T* ro
 }
 
 // --------------------------------------------------------------------------------------
-// Consumers: finish one row after its stages were reduced.
+// Consumers: finish one row after its stages were reduced.  Returns true (every thread)
+// when a bounded wait of the row gave up: nothing is written, the kernel stops.
 // --------------------------------------------------------------------------------------
 template <typename T>
-__device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, const RowPlan& plan,
-                           ThreadAcc& acc) {
+__device__ bool finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, const RowPlan& plan,
+                           ThreadAcc& acc, int w_on, uint32_t w_top16, uint32_t w_nb) {
   const Group g{kCons, kConsBar};
   const int t = threadIdx.x, w = t >> 5, l = t & 31;
   const int64_t V = A.io.V;
@@ -706,9 +699,9 @@ __device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, con
   const T* row = row_ptr<T>(A, row_id);
   const RowLayout L = row_layout(row, V);
   acc_scalars_mode<T>(x.mode, acc, row, L, V, x.c);
-  if (x.window && sh.win_on) {  // the row's unaligned ends go into the window too
-    for (int64_t j = t; j < L.head; j += kCons) win_scalar(sh, load_bits(row, j));
-    for (int64_t j = L.tail0 + t; j < V; j += kCons) win_scalar(sh, load_bits(row, j));
+  if (x.window && w_on) {  // the row's unaligned ends go into the window too
+    for (int64_t j = t; j < L.head; j += kCons) win_scalar(sh, load_bits(row, j), w_top16, w_nb);
+    for (int64_t j = L.tail0 + t; j < V; j += kCons) win_scalar(sh, load_bits(row, j), w_top16, w_nb);
   }
   // warp merge (fixed butterfly), then the warps in order
   const float wfm = warp_reduce(acc.fm, [](float a, float b) { return fmax_nan(a, b); });
@@ -717,6 +710,7 @@ __device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, con
   const long long wam = warp_min_i64(acc.fm == wfm ? acc.amax : LLONG_MAX);
   if (l == 0) { sh.w_fm[w] = wfm; sh.w_s[w] = ws; sh.w_amax[w] = wam; }
   g.sync();  // partials and the window histogram are complete
+  if (sh.abort) return true;
   const bool filt = x.topk || x.topp;
   auto is_bad = [&](float lm, float s) {
     return (lm != lm || lm == INFINITY || lm == -INFINITY) || (x.need_sum && !(s < INFINITY));
@@ -736,9 +730,9 @@ __device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, con
     }
     lmax = fm; s_all = s; amax = am;
     th.s_kept = s_all;
-    if (filt && !is_bad(lmax, s_all) && x.window && sh.win_on) {
+    if (filt && !is_bad(lmax, s_all) && x.window && w_on) {
       const uint32_t kmax16 = order_key(__float_as_uint(lmax)) >> 16;
-      const uint32_t top16 = sh.win_top16, lo16 = top16 - (uint32_t)(sh.win_nb - 1);
+      const uint32_t top16 = w_top16, lo16 = top16 - (w_nb - 1u);
       if (kmax16 >= lo16 && kmax16 <= top16)
         done = warp_select(x, lmax, s_all, sh.hist + (top16 - kmax16), kmax16, (int)(kmax16 - lo16 + 1), th);
     }
@@ -825,7 +819,8 @@ __device__ void finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, con
       A.pub[row_id] = q;
     }
   }
-  g.sync();  // shared scratch of this row is free again after this point
+  // no closing barrier: the next row's first barrier orders every later use of the scratch
+  return false;
 }
 
 // A row claimed by the producer warp.
@@ -960,54 +955,52 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       uint32_t xbits = 0u;
       if (t == 0 && want_x) xbits = load_bits(row, plan.xt);
       bool fail = false;
+      // the row's window (every thread holds the same copy; thread 0 also leaves it in
+      // shared memory for finish_row)
+      int w_on = 0, w_pos = 0;
+      uint32_t w_top16 = 0u, w_nb = 0u;
       for (int c = 0; c < plan.nchunks; ++c) {
         if (c > 0 && !mbar_wait(&sh.full[stage], phase, kWaitPolls)) { fail = true; break; }
         const long long off = (long long)c * kChunk;
         const int nv = (int)(max(0ll, min((long long)kChunk, L.nvec * 16 - off)) / 16);
         const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)stage * kChunk);
         const long long id0 = L.head + (off / 16) * Elem<T>::kPerVec;
-        if (!x.window || (c > 0 && !sh.win_on)) {
+        if (!x.window || (c > 0 && !w_on)) {
           acc_stage_mode<T, 0>(x.mode, acc, sh, sv, nv, id0, x.c);
         } else if (c > 0) {
-          if (sh.win_pos) acc_stage_mode<T, 1>(x.mode, acc, sh, sv, nv, id0, x.c);
-          else acc_stage_mode<T, 2>(x.mode, acc, sh, sv, nv, id0, x.c);
+          if (w_pos) acc_stage_mode<T, 1>(x.mode, acc, sh, sv, nv, id0, x.c, w_top16 - 0x8000u, w_nb);
+          else acc_stage_mode<T, 2>(x.mode, acc, sh, sv, nv, id0, x.c, w_top16, w_nb);
         } else {
           acc_stage_mode<T, 0>(x.mode, acc, sh, sv, nv, id0, x.c);
           // anchor: the maximum of the first stage; the window keeps every token within dz
           // nats of it, and room for values up to 2047 bf16 steps above its bottom
           const float wm = warp_reduce(acc.fm, [](float a, float b) { return fmax_nan(a, b); });
-          if (l == 0) sh.w_fm[w] = wm;
-          g.sync();
-          if (t == 0) {
-            float m0 = -INFINITY;
-            for (int i = 0; i < kConsWarps; ++i) m0 = fmax_nan(m0, sh.w_fm[i]);
-            const float dz = x.topp ? 11.f : 8.f;
-            const float lo = m0 - dz * x.inv_scale;
-            sh.win_on = (m0 == m0 && m0 > -INFINITY && m0 < INFINITY && lo > -3.0e38f) ? 1 : 0;
-            if (sh.win_on) {
-              uint32_t lo16 = order_key(__float_as_uint(lo)) >> 16;
-              lo16 = lo16 > (kKeyNegInf >> 16) ? lo16 - 1 : (kKeyNegInf >> 16);
-              const uint32_t top16 = min(lo16 + (uint32_t)(kWindowBins - 1), 0xFF7Fu);
-              sh.win_lo = key_value(lo16 << 16);
-              sh.win_top16 = top16;
-              sh.win_nb = (int)(top16 - lo16 + 1);
-              sh.win_pos = lo16 > 0x8000u ? 1 : 0;
-              sh.win_hih = (int)top16 - 0x8000;
-            }
+          if (l == 0) sh.w_m0[w] = wm;
+          g.sync();  // the window histogram was cleared before this barrier too
+          float m0 = -INFINITY;
+          for (int i = 0; i < kConsWarps; ++i) m0 = fmax_nan(m0, sh.w_m0[i]);
+          const float dz = x.topp ? 11.f : 8.f;
+          const float lo = m0 - dz * x.inv_scale;
+          w_on = (m0 == m0 && m0 > -INFINITY && m0 < INFINITY && lo > -3.0e38f) ? 1 : 0;
+          if (w_on) {
+            uint32_t lo16 = order_key(__float_as_uint(lo)) >> 16;
+            lo16 = lo16 > (kKeyNegInf >> 16) ? lo16 - 1 : (kKeyNegInf >> 16);
+            w_top16 = min(lo16 + (uint32_t)(kWindowBins - 1), 0xFF7Fu);
+            w_nb = w_top16 - lo16 + 1u;
+            w_pos = lo16 > 0x8000u ? 1 : 0;
+            window_stage<T>(sh, sv, nv, w_pos != 0, w_pos ? w_top16 - 0x8000u : w_top16, w_nb);
           }
-          g.sync();
-          if (sh.win_on) window_stage<T>(sh, sv, nv);
+
         }
         __syncwarp();
         if (l == 0) mbar_arrive(&sh.empty[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (t == 0) sh.xbits = xbits;  // read by finish_row after its first barrier
-      if (fail) sh.abort = 1;
-      g.sync();
-      if (sh.abort) break;
-      finish_row<T>(A, sh, x, plan, acc);
+      if (fail) sh.abort = 1;        // read by finish_row after its first barrier
+      const bool aborted = finish_row<T>(A, sh, x, plan, acc, w_on, w_top16, w_nb);
       acc.reset();
+      if (aborted) break;
     }
     if (t == 0 && sh.abort) atomicOr(&A.hdr->error, 1u);
   }
