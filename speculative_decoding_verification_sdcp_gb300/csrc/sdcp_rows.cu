@@ -145,8 +145,13 @@ __device__ __forceinline__ float acc_vector(ThreadAcc& a, const uint4& q, long l
 // window's values (negative values have h < 0, values above the top give d < 0).  Other
 // windows go through the order key: d = top16 - key16.
 // --------------------------------------------------------------------------------------
+// hist[d] += 1 when d < nb, as a predicated shared-memory reduction (no branch per element).
+__device__ __forceinline__ void hist_add_if(uint32_t hist_base, uint32_t d, uint32_t nb) {
+  asm volatile("{ .reg .pred q; setp.lt.u32 q, %1, %2; @q red.shared.add.u32 [%0], 1; }"
+               ::"r"(hist_base + 4u * d), "r"(d), "r"(nb) : "memory");
+}
 template <bool POS>
-__device__ __forceinline__ void win_word(uint32_t* hist, uint32_t wd, uint32_t top, uint32_t nb) {
+__device__ __forceinline__ void win_word(uint32_t hist_base, uint32_t wd, uint32_t top, uint32_t nb) {
   uint32_t d0, d1;
   if (POS) {
     d0 = top - (uint32_t)((int32_t)(wd << 16) >> 16);
@@ -155,16 +160,17 @@ __device__ __forceinline__ void win_word(uint32_t* hist, uint32_t wd, uint32_t t
     d0 = top - (order_key(wd << 16) >> 16);
     d1 = top - (order_key(wd & 0xFFFF0000u) >> 16);
   }
-  if (d0 < nb) atomicAdd(hist + d0, 1u);
-  if (d1 < nb) atomicAdd(hist + d1, 1u);
+  hist_add_if(hist_base, d0, nb);
+  hist_add_if(hist_base, d1, nb);
 }
 template <typename T, bool POS>
 __device__ __forceinline__ void win_vector(uint32_t* hist, const uint4& q, uint32_t top, uint32_t nb) {
   if constexpr (sizeof(T) == 2) {
-    win_word<POS>(hist, q.x, top, nb);
-    win_word<POS>(hist, q.y, top, nb);
-    win_word<POS>(hist, q.z, top, nb);
-    win_word<POS>(hist, q.w, top, nb);
+    const uint32_t hb = smem_u32(hist);
+    win_word<POS>(hb, q.x, top, nb);
+    win_word<POS>(hb, q.y, top, nb);
+    win_word<POS>(hb, q.z, top, nb);
+    win_word<POS>(hb, q.w, top, nb);
   }
 }
 // One element (bits of a bf16 value in the upper half) of the row's unaligned ends.
