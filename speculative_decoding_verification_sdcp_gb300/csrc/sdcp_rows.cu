@@ -15,11 +15,12 @@
 //
 // Top-k / top-p on bf16 rows: all tokens that share a bf16 value have the same
 // probability, so the exact count of every value in a window below the row maximum decides
-// both cuts (the mass of a value is count * exp(v - max)).  The window (Dz nats below the
-// maximum of the row's first stage: 8 for top-k, 11 for top-p) is counted while the row
-// streams, with a shared-memory histogram of up to 2048 values that every element updates
-// under a predicate (no divergence); one warp then scans the bins for the k-th token and
-// the top-p crossing.  A cut inside one value keeps its first tokens in id order; only
+// both cuts (the mass of a value is count * exp(v - max)).  The window (8 nats below the
+// maximum of the row's first stage) is counted while the row streams, with a shared-memory
+// histogram of up to 2048 values: the stage loop marks the vectors whose maximum reaches
+// the window, each warp lists its marked vectors and counts them one vector per lane with
+// full-warp reductions; one warp then scans the bins for the k-th token and the top-p
+// crossing.  A cut inside one value keeps its first tokens in id order; only
 // their number is recorded.  Rows the window cannot decide are searched again from L2
 // (wider windows, then a bisection over the order-key space).
 #include <climits>
@@ -64,6 +65,8 @@ struct RowShared {
   uint32_t r_thr_key;
   int r_kept, r_done, r_fallback;
   uint32_t hist[kWindowBins];
+  uint32_t hist_pad[32];  // one word per lane: where a lane with nothing to count adds 0
+  uint16_t hits[kConsWarps][kVecPerThread * 32];  // per warp: stage vectors that reach the window
 };
 
 // --------------------------------------------------------------------------------------
@@ -145,13 +148,17 @@ __device__ __forceinline__ float acc_vector(ThreadAcc& a, const uint4& q, long l
 // window's values (negative values have h < 0, values above the top give d < 0).  Other
 // windows go through the order key: d = top16 - key16.
 // --------------------------------------------------------------------------------------
-// hist[d] += 1 when d < nb, as a predicated shared-memory reduction (no branch per element).
-__device__ __forceinline__ void hist_add_if(uint32_t hist_base, uint32_t d, uint32_t nb) {
-  asm volatile("{ .reg .pred q; setp.lt.u32 q, %1, %2; @q red.shared.add.u32 [%0], 1; }"
-               ::"r"(hist_base + 4u * d), "r"(d), "r"(nb) : "memory");
+// hist[d] += 1 when d < nb, else pad[lane] += 0: every lane takes part in every reduction
+// (shared-memory reductions with some lanes masked off cost about twice a full-warp one;
+// the pad words are one per bank, so lanes with nothing to count add no conflicts).
+__device__ __forceinline__ void hist_add_if(uint32_t hist_base, uint32_t pad_lane, uint32_t d, uint32_t nb) {
+  const bool in = d < nb;
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(in ? hist_base + 4u * d : pad_lane), "r"(in ? 1u : 0u)
+               : "memory");
 }
 template <bool POS>
-__device__ __forceinline__ void win_word(uint32_t hist_base, uint32_t wd, uint32_t top, uint32_t nb) {
+__device__ __forceinline__ void win_word(uint32_t hist_base, uint32_t pad_lane, uint32_t wd, uint32_t top,
+                                         uint32_t nb) {
   uint32_t d0, d1;
   if (POS) {
     d0 = top - (uint32_t)((int32_t)(wd << 16) >> 16);
@@ -160,19 +167,52 @@ __device__ __forceinline__ void win_word(uint32_t hist_base, uint32_t wd, uint32
     d0 = top - (order_key(wd << 16) >> 16);
     d1 = top - (order_key(wd & 0xFFFF0000u) >> 16);
   }
-  hist_add_if(hist_base, d0, nb);
-  hist_add_if(hist_base, d1, nb);
+  hist_add_if(hist_base, pad_lane, d0, nb);
+  hist_add_if(hist_base, pad_lane, d1, nb);
 }
-template <typename T, bool POS>
-__device__ __forceinline__ void win_vector(uint32_t* hist, const uint4& q, uint32_t top, uint32_t nb) {
-  if constexpr (sizeof(T) == 2) {
-    const uint32_t hb = smem_u32(hist);
-    win_word<POS>(hb, q.x, top, nb);
-    win_word<POS>(hb, q.y, top, nb);
-    win_word<POS>(hb, q.z, top, nb);
-    win_word<POS>(hb, q.w, top, nb);
+// The row's window as the stage loop carries it.  The stage loop only marks, per thread,
+// the vectors whose maximum reaches the lowest bin (one compare per vector); each warp then
+// lists its marked vectors and counts them 32 at a time, one vector per lane, so the
+// per-element reductions run for marked vectors only.
+struct Window {
+  uint32_t top, nb;  // win_word's top (positive windows: top16 - 0x8000) and bin count
+  float bot;         // value of the lowest bin: every element in the window is >= bot
+};
+// hm: bit i marks vector threadIdx.x + i * kCons of the stage sv.
+template <bool POS>
+__device__ __forceinline__ void win_hits(RowShared& sh, const uint4* sv, uint32_t hm, const Window& wn) {
+  const int l = threadIdx.x & 31;
+  const uint32_t n = (uint32_t)__popc(hm);
+  uint32_t incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (l >= o) incl += v;
   }
+  const uint32_t H = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  if (H == 0u) return;
+  uint16_t* list = sh.hits[threadIdx.x >> 5];
+  uint32_t pos = incl - n;
+  while (hm != 0u) {
+    const int i = __ffs(hm) - 1;
+    hm &= hm - 1u;
+    list[pos++] = (uint16_t)(threadIdx.x + i * kCons);
+  }
+  __syncwarp();
+  const uint32_t hb = smem_u32(sh.hist), pl = smem_u32(sh.hist_pad + l);
+  // every lane runs every round (lanes past H count a vector of -inf, which has no bin)
+  const uint4 none = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+  for (uint32_t e0 = 0; e0 < H; e0 += 32) {
+    const uint32_t e = e0 + (uint32_t)l;
+    const uint4 q = (e < H) ? sv[list[e]] : none;
+    win_word<POS>(hb, pl, q.x, wn.top, wn.nb);
+    win_word<POS>(hb, pl, q.y, wn.top, wn.nb);
+    win_word<POS>(hb, pl, q.z, wn.top, wn.nb);
+    win_word<POS>(hb, pl, q.w, wn.top, wn.nb);
+  }
+  __syncwarp();  // the list is free for the next stage
 }
+
 // One element (bits of a bf16 value in the upper half) of the row's unaligned ends.
 __device__ __forceinline__ void win_scalar(RowShared& sh, uint32_t bits, uint32_t top16, uint32_t nb) {
   const uint32_t d = top16 - (order_key(bits) >> 16);
@@ -180,16 +220,17 @@ __device__ __forceinline__ void win_scalar(RowShared& sh, uint32_t bits, uint32_
 }
 
 // Vectors [0, nv) of one ring stage (nv <= kVecPerThread * kCons); vector v is element
-// id0 + v * E of the row and belongs to consumer thread v % kCons.  WIN 1 / 2: count the
-// stage into the window (positive / general indexing).  Vectors past nv read as -inf, which
-// changes no statistic and no bin.
-template <typename T, bool ARGMAX, bool SUM, int WIN>
-__device__ __forceinline__ void acc_stage(ThreadAcc& a, RowShared& sh, const uint4* sv, int nv,
-                                          long long id0, float c, uint32_t top, uint32_t nb) {
+// id0 + v * E of the row and belongs to consumer thread v % kCons.  WIN: returns the mask of
+// the thread's vectors whose maximum is >= bot (bit i: vector t + i * kCons).  Vectors past
+// nv read as -inf, which changes no statistic and marks nothing.
+template <typename T, bool ARGMAX, bool SUM, bool WIN>
+__device__ __forceinline__ uint32_t acc_stage(ThreadAcc& a, const uint4* sv, int nv, long long id0, float c,
+                                              float bot) {
   constexpr int E = Elem<T>::kPerVec;
   const int t = threadIdx.x;
   const uint32_t ninf = (sizeof(T) == 2) ? 0xFF80FF80u : 0xFF800000u;
   const uint4 pad = make_uint4(ninf, ninf, ninf, ninf);
+  uint32_t hm = 0u;
 #pragma unroll 1
   for (int i0 = 0; i0 < kVecPerThread; i0 += 4) {
     uint4 q[4];
@@ -201,27 +242,24 @@ __device__ __forceinline__ void acc_stage(ThreadAcc& a, RowShared& sh, const uin
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int v = t + (i0 + u) * kCons;
-      acc_vector<T, ARGMAX, SUM>(a, q[u], id0 + (long long)v * E, c);
-      if (WIN == 1) win_vector<T, true>(sh.hist, q[u], top, nb);
-      if (WIN == 2) win_vector<T, false>(sh.hist, q[u], top, nb);
+      const float vm = acc_vector<T, ARGMAX, SUM>(a, q[u], id0 + (long long)v * E, c);
+      if (WIN) hm |= (vm >= bot ? 1u : 0u) << (i0 + u);
     }
   }
+  return hm;
 }
 
-// The window over a stage that was reduced before the window was placed (the first).
+// The marks of a stage that was reduced before the window was placed (the first).
 template <typename T>
-__device__ __forceinline__ void window_stage(RowShared& sh, const uint4* sv, int nv, bool pos, uint32_t top,
-                                             uint32_t nb) {
+__device__ __forceinline__ uint32_t window_marks(const uint4* sv, int nv, float bot) {
   const int t = threadIdx.x;
-#pragma unroll 4
+  uint32_t hm = 0u;
+#pragma unroll
   for (int i = 0; i < kVecPerThread; ++i) {
     const int v = t + i * kCons;
-    if (v < nv) {
-      const uint4 q = sv[v];
-      if (pos) win_vector<T, true>(sh.hist, q, top, nb);
-      else win_vector<T, false>(sh.hist, q, top, nb);
-    }
+    if (v < nv && vec_max(sv[v], T()) >= bot) hm |= 1u << i;
   }
+  return hm;
 }
 
 template <typename T, bool ARGMAX, bool SUM>
@@ -233,14 +271,14 @@ __device__ __forceinline__ void acc_scalars(ThreadAcc& a, const T* row, const Ro
 // Row modes: which statistics a row needs.
 enum RowMode { kModeMax = 0, kModeArgmax = 1, kModeSum = 2, kModeArgmaxSum = 3 };
 
-template <typename T, int WIN>
-__device__ __forceinline__ void acc_stage_mode(int mode, ThreadAcc& a, RowShared& sh, const uint4* sv, int nv,
-                                               long long id0, float c, uint32_t top = 0u, uint32_t nb = 0u) {
+template <typename T, bool WIN>
+__device__ __forceinline__ uint32_t acc_stage_mode(int mode, ThreadAcc& a, const uint4* sv, int nv, long long id0,
+                                                   float c, float bot = 0.f) {
   switch (mode) {
-    case kModeMax: acc_stage<T, false, false, WIN>(a, sh, sv, nv, id0, c, top, nb); break;
-    case kModeArgmax: acc_stage<T, true, false, WIN>(a, sh, sv, nv, id0, c, top, nb); break;
-    case kModeSum: acc_stage<T, false, true, WIN>(a, sh, sv, nv, id0, c, top, nb); break;
-    default: acc_stage<T, true, true, WIN>(a, sh, sv, nv, id0, c, top, nb); break;
+    case kModeMax: return acc_stage<T, false, false, WIN>(a, sv, nv, id0, c, bot);
+    case kModeArgmax: return acc_stage<T, true, false, WIN>(a, sv, nv, id0, c, bot);
+    case kModeSum: return acc_stage<T, false, true, WIN>(a, sv, nv, id0, c, bot);
+    default: return acc_stage<T, true, true, WIN>(a, sv, nv, id0, c, bot);
   }
 }
 template <typename T>
@@ -570,16 +608,11 @@ __device__ bool window_thresholds(const Group& g, RowShared& sh, const T* row, c
   g.sync();  // earlier readers of the histogram are done
   for (int i = t; i < kWindowBins; i += kCons) sh.hist[i] = 0u;
   g.sync();
-  const uint32_t klo16 = kmax16 - (uint32_t)(nb - 1);
-  const float wbot = key_value(klo16 << 16);
-  scan_row<T>(row, L, V, [&](const uint32_t (&b)[Elem<T>::kPerVec], long long id0, int n) {
-    float vm = -INFINITY;
+  const uint32_t hb = smem_u32(sh.hist), pl = smem_u32(sh.hist_pad + (t & 31));
+  scan_row<T>(row, L, V, [&](const uint32_t (&b)[Elem<T>::kPerVec], long long, int n) {
 #pragma unroll
-    for (int e = 0; e < Elem<T>::kPerVec; ++e) vm = fmaxf(vm, __uint_as_float(b[e]));
-    if (vm >= wbot) {
-      for (int e = 0; e < n; ++e)
-        if (__uint_as_float(b[e]) >= wbot) atomicAdd(&sh.hist[kmax16 - (order_key(b[e]) >> 16)], 1u);
-    }
+    for (int e = 0; e < Elem<T>::kPerVec; ++e)
+      hist_add_if(hb, pl, e < n ? kmax16 - (order_key(b[e]) >> 16) : (uint32_t)nb, (uint32_t)nb);
   });
   g.sync();
   if ((t >> 5) == 0) {
@@ -751,9 +784,9 @@ __device__ bool finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, con
     if (!is_bad(lmax, s_all) && !done) {
       th = Thresholds{0u, LLONG_MAX, (int)V, s_all, false};
       if (sizeof(T) == 2) {
-        // the k-th token of top-k lies a few nats below the maximum, the top-p crossing of
-        // a broad distribution deeper
-        const float dz1 = x.topp ? 11.f : 8.f;
+        // the streamed window (8 nats below the first stage's maximum) missed the cut: 12
+        // nats below the row maximum, then 24, then the 2048 values below it
+        const float dz1 = 12.f;
         done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, dz1, th);
         if (!done) done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, 2.f * dz1, th);
         if (!done) done = window_thresholds<T>(g, sh, row, L, x, V, lmax, s_all, 0.f, th);
@@ -965,6 +998,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       // shared memory for finish_row)
       int w_on = 0, w_pos = 0;
       uint32_t w_top16 = 0u, w_nb = 0u;
+      Window wn{0u, 0u, 0.f};
       for (int c = 0; c < plan.nchunks; ++c) {
         if (c > 0 && !mbar_wait(&sh.full[stage], phase, kWaitPolls)) { fail = true; break; }
         const long long off = (long long)c * kChunk;
@@ -972,12 +1006,13 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
         const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)stage * kChunk);
         const long long id0 = L.head + (off / 16) * Elem<T>::kPerVec;
         if (!x.window || (c > 0 && !w_on)) {
-          acc_stage_mode<T, 0>(x.mode, acc, sh, sv, nv, id0, x.c);
+          acc_stage_mode<T, false>(x.mode, acc, sv, nv, id0, x.c);
         } else if (c > 0) {
-          if (w_pos) acc_stage_mode<T, 1>(x.mode, acc, sh, sv, nv, id0, x.c, w_top16 - 0x8000u, w_nb);
-          else acc_stage_mode<T, 2>(x.mode, acc, sh, sv, nv, id0, x.c, w_top16, w_nb);
+          const uint32_t hm = acc_stage_mode<T, true>(x.mode, acc, sv, nv, id0, x.c, wn.bot);
+          if (w_pos) win_hits<true>(sh, sv, hm, wn);
+          else win_hits<false>(sh, sv, hm, wn);
         } else {
-          acc_stage_mode<T, 0>(x.mode, acc, sh, sv, nv, id0, x.c);
+          acc_stage_mode<T, false>(x.mode, acc, sv, nv, id0, x.c);
           // anchor: the maximum of the first stage; the window keeps every token within dz
           // nats of it, and room for values up to 2047 bf16 steps above its bottom
           const float wm = warp_reduce(acc.fm, [](float a, float b) { return fmax_nan(a, b); });
@@ -985,7 +1020,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
           g.sync();  // the window histogram was cleared before this barrier too
           float m0 = -INFINITY;
           for (int i = 0; i < kConsWarps; ++i) m0 = fmax_nan(m0, sh.w_m0[i]);
-          const float dz = x.topp ? 11.f : 8.f;
+          const float dz = 8.f;
           const float lo = m0 - dz * x.inv_scale;
           w_on = (m0 == m0 && m0 > -INFINITY && m0 < INFINITY && lo > -3.0e38f) ? 1 : 0;
           if (w_on) {
@@ -994,7 +1029,10 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
             w_top16 = min(lo16 + (uint32_t)(kWindowBins - 1), 0xFF7Fu);
             w_nb = w_top16 - lo16 + 1u;
             w_pos = lo16 > 0x8000u ? 1 : 0;
-            window_stage<T>(sh, sv, nv, w_pos != 0, w_pos ? w_top16 - 0x8000u : w_top16, w_nb);
+            wn = Window{w_pos ? w_top16 - 0x8000u : w_top16, w_nb, key_value(lo16 << 16)};
+            const uint32_t hm = window_marks<T>(sv, nv, wn.bot);
+            if (w_pos) win_hits<true>(sh, sv, hm, wn);
+            else win_hits<false>(sh, sv, hm, wn);
           }
 
         }
