@@ -41,11 +41,19 @@ constexpr int kRowCtasPerSm = 2;
 constexpr int kVecPerThread = kChunk / 16 / kCons;
 static_assert(kCons == kThreads, "the consumer group runs session completions");
 
+// What a row needs, from its session (resolved once, by the producer warp).
+struct RowCtx {
+  float c, inv_scale;  // log2(e) 1000/T; T/1000
+  uint32_t top_k, top_p_milli, temperature_milli;
+  int mode;
+  bool has_x, one_hot, topk, topp, need_keys, need_sum, window;
+};
+
 struct RowPlan {
   long long row_id;  // < 0: no more work for the CTA
-  int b;
   int nchunks;
   int32_t xt;        // the row's draft token as the token array holds it (-1: none)
+  RowCtx x;
 };
 
 struct RowShared {
@@ -293,51 +301,47 @@ __device__ __forceinline__ void acc_scalars_mode(int mode, ThreadAcc& a, const T
 }
 
 // --------------------------------------------------------------------------------------
-// What a row needs, from its session (identical for the producer and the consumers).
+// What a row needs, from its session.
 // --------------------------------------------------------------------------------------
-struct RowCtx {
-  bool skip, is_target, has_x, one_hot, topk, topp, need_keys, need_sum, need_max, window;
-  int b;
-  long long tok_idx;
-  float c, inv_scale;  // log2(e) 1000/T; T/1000
-  sdcp_session_params P;
-  int mode;
-};
 
-__device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, int b, bool bf16) {
+// Row row_id of session b; skip: the row needs no statistics; tok_idx: its draft token's
+// index in the token array (when has_x).
+__device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, int b, bool bf16, bool& skip,
+                                          long long& tok_idx) {
   RowCtx x;
   const long long R_T = A.io.total + A.io.B;
-  x.is_target = row_id < R_T;
-  x.b = b;
-  x.P = A.io.params[b];
+  const bool is_target = row_id < R_T;
+  const sdcp_session_params P = A.io.params[b];
   const long long off0 = A.io.m_offsets[b], off1 = A.io.m_offsets[b + 1];
   const long long M = off1 - off0;
-  const long long pos = x.is_target ? row_id - off0 - b : (row_id - R_T) - off0;
-  x.tok_idx = x.is_target ? row_id - b : row_id - R_T;
-  x.has_x = (pos >= 0 && pos < M && x.tok_idx >= 0 && x.tok_idx < A.io.total);
-  const bool params_ok = (x.P.top_p_milli <= 1000u);
-  const bool session_ok = params_ok && (x.P.rule_id == 1u || x.P.rule_id == 2u) && M >= 1 &&
+  const long long pos = is_target ? row_id - off0 - b : (row_id - R_T) - off0;
+  tok_idx = is_target ? row_id - b : row_id - R_T;
+  x.has_x = (pos >= 0 && pos < M && tok_idx >= 0 && tok_idx < A.io.total);
+  const bool params_ok = (P.top_p_milli <= 1000u);
+  const bool session_ok = params_ok && (P.rule_id == 1u || P.rule_id == 2u) && M >= 1 &&
                           M <= SDCP_MAX_M && off0 >= 0 && off1 <= A.io.total;
   bool want_argmax, want_profile;
   if (A.stats_mode) {
-    x.skip = !params_ok;
+    skip = !params_ok;
     want_argmax = true;
     want_profile = true;
   } else {
-    const bool rule2 = (x.P.rule_id == 2u);
-    x.skip = !session_ok || (!x.is_target && !rule2) || (!x.is_target && A.io.draft == nullptr);
-    want_argmax = !rule2 || x.P.temperature_milli == 0u;
-    want_profile = rule2 && x.P.temperature_milli != 0u;
+    const bool rule2 = (P.rule_id == 2u);
+    skip = !session_ok || (!is_target && !rule2) || (!is_target && A.io.draft == nullptr);
+    want_argmax = !rule2 || P.temperature_milli == 0u;
+    want_profile = rule2 && P.temperature_milli != 0u;
   }
-  const uint32_t tm = x.P.temperature_milli;
+  const uint32_t tm = P.temperature_milli;
+  x.top_k = P.top_k;
+  x.top_p_milli = P.top_p_milli;
+  x.temperature_milli = tm;
   x.one_hot = (tm == 0u);
   x.c = x.one_hot ? 0.f : profile_c(tm);
   x.inv_scale = profile_inv_scale(tm);
-  x.topk = !x.one_hot && want_profile && x.P.top_k != 0u && (int64_t)x.P.top_k < A.io.V;
-  x.topp = !x.one_hot && want_profile && x.P.top_p_milli < 1000u;
+  x.topk = !x.one_hot && want_profile && P.top_k != 0u && (int64_t)P.top_k < A.io.V;
+  x.topp = !x.one_hot && want_profile && P.top_p_milli < 1000u;
   x.need_keys = want_argmax || x.one_hot;  // the argmax is needed
   x.need_sum = want_profile && !x.one_hot && !x.topk;
-  x.need_max = want_profile && !x.one_hot;
   x.mode = x.need_keys ? (x.need_sum ? kModeArgmaxSum : kModeArgmax) : (x.need_sum ? kModeSum : kModeMax);
   x.window = (x.topk || x.topp) && bf16;
   return x;
@@ -494,7 +498,7 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
   if (l == 0) { cpre = 0; mpre = 0.f; }
   int dk = nb, tk = 0;
   float s_base = s_all;  // mass of the set the nucleus is taken from
-  const long long k = x.P.top_k;
+  const long long k = x.top_k;
   if (x.topk) {
     const unsigned m = __ballot_sync(0xFFFFFFFFu, cpre < k && k <= cpre + cnt);
     if (m == 0u) return false;  // fewer than k tokens in the window
@@ -519,7 +523,7 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
   }
   int dcut = dk, ncut = tk;
   if (x.topp) {
-    const float target = (float)x.P.top_p_milli * 0.001f * s_base;
+    const float target = (float)x.top_p_milli * 0.001f * s_base;
     int cd = -1, cn = 0;
     float cb = 0.f;
     long long ccb = 0;
@@ -638,7 +642,7 @@ __device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, 
   uint32_t kk1 = 0u;
   long long id1 = LLONG_MAX, k1count = V;
   if (x.topk) {
-    const long long k = x.P.top_k;
+    const long long k = x.top_k;
     uint32_t lo = 0u, hi = kmax_f;
     while (lo < hi) {
       const uint32_t mid = lo + (uint32_t)(((uint64_t)hi - lo + 1) / 2);
@@ -666,7 +670,7 @@ __device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, 
   const float s1 = mass_ge(0u);
   float skept = s1;
   if (x.topp) {
-    const float target = (float)x.P.top_p_milli * 0.001f * s1;
+    const float target = (float)x.top_p_milli * 0.001f * s1;
     uint32_t lo = 0u, hi = kmax_f;
     while (lo < hi) {
       const uint32_t mid = lo + (uint32_t)(((uint64_t)hi - lo + 1) / 2);
@@ -854,7 +858,7 @@ __device__ bool finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, con
       if (!(flags & kRowHasX)) q.lp_x = __int_as_float(0x7FC00000);
       else if (!(flags & SDCP_ROW_X_KEPT)) q.lp_x = -INFINITY;
       else if (x.one_hot) q.lp_x = 0.f;
-      else q.lp_x = (float)((double)st.dlx * (1000.0 / (double)x.P.temperature_milli) - log((double)st.s));
+      else q.lp_x = (float)((double)st.dlx * (1000.0 / (double)x.temperature_milli) - log((double)st.s));
       A.pub[row_id] = q;
     }
   }
@@ -865,25 +869,27 @@ __device__ bool finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, con
 // A row claimed by the producer warp.
 struct SlotInfo {
   long long row_id;  // -1: none
-  int b;
   bool skip;
   int32_t xt;        // the row's draft token (-1: none)
+  RowCtx x;
 };
 
 // Row r (whole warp): its session and what it needs.
 template <typename T>
 __device__ SlotInfo resolve_row(const RowArgs& A, long long r) {
-  SlotInfo s{-1, 0, true, -1};
+  SlotInfo s;
+  s.row_id = -1;
+  s.skip = true;
+  s.xt = -1;
   const SessIO& io = A.io;
   const long long R_T = io.total + io.B;
   if (r >= R_T + io.total) return s;
   const bool is_target = r < R_T;
   const int32_t b = find_session(io.m_offsets, io.B, is_target ? r : r - R_T, is_target);
-  const RowCtx x = row_ctx(A, r, b, sizeof(T) == 2);
+  long long tok_idx = 0;
+  s.x = row_ctx(A, r, b, sizeof(T) == 2, s.skip, tok_idx);
   s.row_id = r;
-  s.b = b;
-  s.skip = x.skip;
-  s.xt = x.has_x ? io.tokens[x.tok_idx] : -1;
+  s.xt = s.x.has_x ? io.tokens[tok_idx] : -1;
   return s;
 }
 
@@ -930,7 +936,10 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       const int nch = (int)max(1ll, (vbytes + kChunk - 1) / kChunk);
       const char* src = reinterpret_cast<const char*>(row + L.head);
       long long rnext = nrows;
-      SlotInfo nxt{-1, 0, true, -1};
+      SlotInfo nxt;
+      nxt.row_id = -1;
+      nxt.skip = true;
+      nxt.xt = -1;
       for (int c = 0; c < nch && ok; ++c) {
         if (l == 0) {
           if (!mbar_wait(&sh.empty[stage], phase ^ 1u, kWaitPolls) || sh.abort) {
@@ -938,7 +947,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
           } else {
             const long long off = (long long)c * kChunk;
             const uint32_t bytes = (uint32_t)max(0ll, min((long long)kChunk, vbytes - off));
-            if (c == 0) sh.plan[stage] = RowPlan{cur.row_id, cur.b, nch, cur.xt};
+            if (c == 0) sh.plan[stage] = RowPlan{cur.row_id, nch, cur.xt, cur.x};
             mbar_arrive_expect_tx(&sh.full[stage], bytes);
             if (bytes > 0) bulk_copy_g2s(ring + (size_t)stage * kChunk, src + off, bytes, &sh.full[stage]);
           }
@@ -984,7 +993,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       if (sh.abort) break;
       const RowPlan plan = sh.plan[stage];
       if (plan.row_id < 0) break;
-      const RowCtx x = row_ctx(A, plan.row_id, plan.b, sizeof(T) == 2);
+      const RowCtx& x = plan.x;
       const T* row = row_ptr<T>(A, plan.row_id);
       const RowLayout L = row_layout(row, A.io.V);
       if (x.window)  // fresh window for this row (ordered before use by the anchor's barriers)
