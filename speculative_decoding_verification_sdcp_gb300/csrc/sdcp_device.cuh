@@ -287,6 +287,44 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// A waiting thread sleeps until the phase completes or kSuspendNs pass (so a waiting warp
+// takes no issue slots from the warps that work); a wait gives up after kWaitNs in all.
+constexpr uint32_t kSuspendNs = 100000;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+               : "=r"(done) : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs) : "memory");
+  return done != 0;
+}
+// Bounded wait that polls without sleeping (for a warp whose next work is the awaited data).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+}
+// Bounded wait for the phase of `parity`: false after kWaitNs, or at once when *abort is set
+// (another role of the block gave up; abort may be null).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+}
 // Global -> shared bulk copy completing on an mbarrier (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"

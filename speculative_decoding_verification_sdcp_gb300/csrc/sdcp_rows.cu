@@ -36,7 +36,6 @@ constexpr int kRowThreads = kCons + 32;
 constexpr int kStages = 3;
 constexpr int kChunk = 32768;            // bytes per ring stage (8 vectors per consumer thread)
 constexpr int kConsBar = 1;              // named barrier of the consumer warps
-constexpr long long kWaitPolls = 1ll << 22;
 constexpr int kRowCtasPerSm = 2;
 constexpr int kVecPerThread = kChunk / 16 / kCons;
 static_assert(kCons == kThreads, "the consumer group runs session completions");
@@ -942,7 +941,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       nxt.xt = -1;
       for (int c = 0; c < nch && ok; ++c) {
         if (l == 0) {
-          if (!mbar_wait(&sh.empty[stage], phase ^ 1u, kWaitPolls) || sh.abort) {
+          if (!mbar_wait_spin(&sh.empty[stage], phase ^ 1u, &sh.abort) || sh.abort) {
             ok = false;
           } else {
             const long long off = (long long)c * kChunk;
@@ -966,7 +965,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       cur = nxt;
     }
     if (l == 0) {
-      if (ok && mbar_wait(&sh.empty[stage], phase ^ 1u, kWaitPolls) && !sh.abort) {
+      if (ok && mbar_wait_for(&sh.empty[stage], phase ^ 1u, &sh.abort) && !sh.abort) {
         sh.plan[stage].row_id = -1;
         mbar_arrive_expect_tx(&sh.full[stage], 0);
       } else {
@@ -988,7 +987,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
     ThreadAcc acc;
     acc.reset();
     while (true) {
-      if (!mbar_wait(&sh.full[stage], phase, kWaitPolls)) sh.abort = 1;
+      if (!mbar_wait_for(&sh.full[stage], phase, &sh.abort)) sh.abort = 1;
       g.sync();
       if (sh.abort) break;
       const RowPlan plan = sh.plan[stage];
@@ -1009,7 +1008,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       uint32_t w_top16 = 0u, w_nb = 0u;
       Window wn{0u, 0u, 0.f};
       for (int c = 0; c < plan.nchunks; ++c) {
-        if (c > 0 && !mbar_wait(&sh.full[stage], phase, kWaitPolls)) { fail = true; break; }
+        if (c > 0 && !mbar_wait_for(&sh.full[stage], phase, &sh.abort)) { fail = true; break; }
         const long long off = (long long)c * kChunk;
         const int nv = (int)(max(0ll, min((long long)kChunk, L.nvec * 16 - off)) / 16);
         const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)stage * kChunk);

@@ -26,7 +26,6 @@ constexpr int kTieCap = 64;         // tokens on a cut value held per warp (sing
 constexpr int kTieStages = 64;      // stages whose cut-value counts are kept (single-pass draw)
 constexpr int kDrawHalf = 16384;    // bytes of p (and of q) per stage of the streamed draw
 constexpr int kDrawStages = 2;      // stages of the streamed draw's ring
-constexpr long long kDrawPolls = 1ll << 22;
 
 // A token whose keptness depends on its rank among the tokens of a cut value (p's or q's).
 struct TieEntry {
@@ -679,7 +678,7 @@ __device__ float draw_stream(cg::cluster_group& cluster, const Group& g, SessSme
   auto issue = [&](int s) {  // thread 0: stage s of the slice into its slot
     const uint32_t u = use0 + (uint32_t)s;
     const int slot = (int)(u % kDrawStages);
-    if (u >= kDrawStages && !mbar_wait(&sm.empty[slot], ((u / kDrawStages) - 1) & 1u, kDrawPolls)) {
+    if (u >= kDrawStages && !mbar_wait_for(&sm.empty[slot], ((u / kDrawStages) - 1) & 1u, nullptr)) {
       fail = true;
       return;
     }
@@ -697,7 +696,7 @@ __device__ float draw_stream(cg::cluster_group& cluster, const Group& g, SessSme
   for (int s = 0; s < nst; ++s) {
     const uint32_t u = use0 + (uint32_t)s;
     const int slot = (int)(u % kDrawStages);
-    if (!mbar_wait(&sm.full[slot], (u / kDrawStages) & 1u, kDrawPolls)) fail = true;
+    if (!mbar_wait_for(&sm.full[slot], (u / kDrawStages) & 1u, nullptr)) fail = true;
     const unsigned char* src = ring + (size_t)slot * 2 * kDrawHalf;
     const int stage_lo = lo + s * S;
 #pragma unroll 1
