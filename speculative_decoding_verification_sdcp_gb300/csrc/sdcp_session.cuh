@@ -26,6 +26,9 @@ constexpr int kTieCap = 64;         // tokens on a cut value held per warp (sing
 constexpr int kTieStages = 64;      // stages whose cut-value counts are kept (single-pass draw)
 constexpr int kDrawHalf = 16384;    // bytes of p (and of q) per stage of the streamed draw
 constexpr int kDrawStages = 2;      // stages of the streamed draw's ring
+constexpr int kKeptW = 128;         // candidates (p's kept tokens) per warp: kept-set draw
+constexpr int kQCutW = 32;          // q's cut-value ids per warp: kept-set draw
+constexpr int kKeptSliceBytes = 65536;  // largest slice of p a CTA scans with plain loads
 
 // A token whose keptness depends on its rank among the tokens of a cut value (p's or q's).
 struct TieEntry {
@@ -35,11 +38,26 @@ struct TieEntry {
   int lp, lq;  // its index among p's (q's) cut-value tokens of its stage and warp
 };
 
+// The kept-set draw's lists (per warp, in id order) and its per-CTA results.
+struct KeptSmem {
+  int id[kWarps][kKeptW];     // p's candidates: tokens at or above p's cut value
+  float v[kWarps][kKeptW];    // their p logits
+  float r[kWarps][kKeptW];    // their weights (first their q logits)
+  float pre[kWarps][kKeptW];  // running weight sums before them, within the warp
+  int qid[kWarps][kQCutW];    // q's cut-value tokens
+  int n[kWarps], qn[kWarps], pc[kWarps], best[kWarps], last[kWarps];
+  float wsum[kWarps], wbase[kWarps];
+  int cta_ovf, cta_pc, cta_qc, tie_p, tie_q;
+};
+
 // Shared memory of one CTA of a session's cluster (the streamed draw's ring is dynamic).
 struct SessSmem {
   uint64_t full[kDrawStages], empty[kDrawStages];
   float seg[kSegCap];  // per segment group of the CTA's slice: weight sums or tie counts
-  TieEntry ties[kWarps][kTieCap];  // per warp, in id order within each stage
+  union {
+    TieEntry ties[kWarps][kTieCap];  // per warp, in id order within each stage
+    KeptSmem kept;                   // the kept-set draw
+  };
   int tie_n[kWarps];
   int tsc_p[kTieStages][kWarps], tsc_q[kTieStages][kWarps];  // cut-value tokens per stage, warp
   int overflow;
@@ -878,6 +896,241 @@ __device__ int cut_tie_id(cg::cluster_group& cluster, const Group& g, SessSmem& 
   return (id == LLONG_MAX || id == INT_MAX) ? INT_MAX : (int)id;
 }
 
+// ---------------------------------------------------------------------------------
+// The kept-set draw.  When p has a cut (top-k / top-p), every token outside p's kept set
+// has p = 0 and so neither a residual nor a bonus weight: the CTAs scan their slices of p's
+// row for the tokens at or above p's cut value (a compare per token), hold them in per-warp
+// lists in id order, and weigh only those (q is read at their ids alone).  Cut-value ties
+// are ranked from the lists: p's from its own candidates, q's from the ids of q's cut-value
+// tokens collected in the same pass.  Returns W (the same in every CTA), or NaN when some
+// list of the cluster overflowed (the streamed draw takes over).
+// ---------------------------------------------------------------------------------
+
+// Appends the lanes' marked ids (bit e of m: id j0 + e) to a warp list in id order; vals
+// (optional) are the matching logits.  n: the list length (lane-uniform); false on overflow.
+template <int CAP>
+__device__ __forceinline__ bool warp_list_append(int* ids, float* vals, int& n, unsigned m, int j0,
+                                                 const uint32_t (&bits)[kEpt]) {
+  const int lane = threadIdx.x & 31;
+  if (__ballot_sync(0xFFFFFFFFu, m != 0u) == 0u) return true;
+  const int c = __popc(m);
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  if (n + tot > CAP) { n = CAP + 1; return false; }
+  int pos = n + incl - c;
+#pragma unroll
+  for (int e = 0; e < kEpt; ++e)
+    if ((m >> e) & 1u) {
+      ids[pos] = j0 + e;
+      if (vals) vals[pos] = __uint_as_float(bits[e]);
+      ++pos;
+    }
+  n += tot;
+  return true;
+}
+
+// Id of the k-th (1-based, id order) candidate of this CTA with value val: INT_MAX if the
+// CTA holds fewer (one full warp; every lane returns it).
+__device__ __forceinline__ int kth_candidate(const KeptSmem& K, float val, long long k) {
+  const int lane = threadIdx.x & 31;
+  int w = 0;
+  for (; w < kWarps && k > K.pc[w]; ++w) k -= K.pc[w];
+  if (w == kWarps || k < 1) return INT_MAX;
+  for (int i0 = 0; i0 < K.n[w]; i0 += 32) {
+    const int i = i0 + lane;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, i < K.n[w] && K.v[w][i] == val);
+    const int c = __popc(m);
+    if (k <= c) return K.id[w][i0 + (int)__fns(m, 0, (int)k)];
+    k -= c;
+  }
+  return INT_MAX;
+}
+// Id of the k-th (1-based, id order) listed q cut-value token of this CTA (any thread).
+__device__ __forceinline__ int kth_qcut(const KeptSmem& K, long long k) {
+  for (int w = 0; w < kWarps; ++w) {
+    if (k >= 1 && k <= K.qn[w]) return K.qid[w][k - 1];
+    k -= K.qn[w];
+  }
+  return INT_MAX;
+}
+
+template <typename T>
+__device__ float draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem& sm, const T* prow,
+                           const T* qrow, bool residual, bool al_p, bool al_q, int V, DrawRow pr, DrawRow qr,
+                           int np_cut, int nq_cut, double u1, int32_t* out) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
+  const SegSlice sl(V, C, rank);
+  int sa, sb;
+  sl.warp_range(w, kWarps, sa, sb);
+  const bool pp = np_cut != INT_MAX;              // p's cut value is kept in part
+  const bool qp = residual && nq_cut != INT_MAX;  // q's cut value is kept in part
+  KeptSmem& K = sm.kept;
+  // pass: p's candidates and q's cut-value ids of the warp's segments, in id order
+  int nc = 0, nq = 0;
+  constexpr int U = (sizeof(T) == 2) ? 4 : 2;
+  for (int k = sa; k < sb; k += U) {
+    Raw8<T> rp[U], rq[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (k + u < sb) {
+        load_raw8<T>(prow, al_p, V, (k + u) * kSegIds + lane * kEpt, rp[u]);
+        if (qp) load_raw8<T>(qrow, al_q, V, (k + u) * kSegIds + lane * kEpt, rq[u]);
+      }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (k + u >= sb) break;
+      const int j0 = (k + u) * kSegIds + lane * kEpt;
+      uint32_t bb[kEpt];
+      unpack_raw8<T>(rp[u], bb);
+      unsigned m = 0u;
+#pragma unroll
+      for (int e = 0; e < kEpt; ++e) m |= (j0 + e < V && __uint_as_float(bb[e]) >= pr.thr ? 1u : 0u) << e;
+      (void)warp_list_append<kKeptW>(K.id[w], K.v[w], nc, nc > kKeptW ? 0u : m, j0, bb);
+      if (qp) {
+        unpack_raw8<T>(rq[u], bb);
+        unsigned mq = 0u;
+#pragma unroll
+        for (int e = 0; e < kEpt; ++e) mq |= (j0 + e < V && __uint_as_float(bb[e]) == qr.thr ? 1u : 0u) << e;
+        (void)warp_list_append<kQCutW>(K.qid[w], nullptr, nq, nq > kQCutW ? 0u : mq, j0, bb);
+      }
+    }
+  }
+  // p's cut-value candidates of the warp
+  int pc = 0;
+  if (pp && nc <= kKeptW) {
+    for (int i = lane; i < nc; i += 32) pc += (K.v[w][i] == pr.thr) ? 1 : 0;
+    pc = (int)__reduce_add_sync(0xFFFFFFFFu, (unsigned)pc);
+  }
+  if (lane == 0) { K.n[w] = nc; K.qn[w] = nq; K.pc[w] = pc; }
+  g.sync();
+  if (t == 0) {
+    int ovf = 0, tp = 0, tq = 0;
+    for (int i = 0; i < kWarps; ++i) {
+      ovf |= (K.n[i] > kKeptW || K.qn[i] > kQCutW) ? 1 : 0;
+      tp += K.pc[i];
+      tq += K.qn[i];
+    }
+    K.cta_ovf = ovf; K.cta_pc = tp; K.cta_qc = tq;
+    K.tie_p = INT_MAX; K.tie_q = INT_MAX;
+  }
+  int tie_p = INT_MAX, tie_q = INT_MAX;
+  bool bad = false;
+  if (pp || qp) {  // the ids of the np_cut-th / nq_cut-th cut-value tokens over the cluster
+    cluster.sync();
+    long long bp = 0, bq = 0, ap = 0, aq = 0;
+    int op = -1, oq = -1;
+    for (unsigned r = 0; r < C; ++r) {
+      bad |= *cluster.map_shared_rank(&K.cta_ovf, r) != 0;
+      const int cp = *cluster.map_shared_rank(&K.cta_pc, r), cq = *cluster.map_shared_rank(&K.cta_qc, r);
+      if (r == rank) { bp = ap; bq = aq; }
+      if (op < 0 && ap < np_cut && np_cut <= ap + cp) op = (int)r;
+      if (oq < 0 && aq < nq_cut && nq_cut <= aq + cq) oq = (int)r;
+      ap += cp;
+      aq += cq;
+    }
+    if (!bad && w == 0) {
+      if (pp && op == (int)rank) {
+        const int id = kth_candidate(K, pr.thr, np_cut - bp);
+        if (lane == 0) K.tie_p = id;
+      }
+      if (qp && oq == (int)rank && lane == 0) K.tie_q = kth_qcut(K, nq_cut - bq);
+    }
+    cluster.sync();
+    if (pp && op >= 0) tie_p = *cluster.map_shared_rank(&K.tie_p, (unsigned)op);
+    if (qp && oq >= 0) tie_q = *cluster.map_shared_rank(&K.tie_q, (unsigned)oq);
+  }
+  // weights of the warp's candidates, and their running sums in id order
+  pr.tie = pp ? tie_p : INT_MAX;
+  qr.tie = qp ? tie_q : INT_MAX;
+  float run = 0.f;
+  if (!bad && nc <= kKeptW) {
+    if (residual)  // q at the candidates' ids (the loads all in flight at once)
+      for (int i = lane; i < nc; i += 32) K.r[w][i] = __uint_as_float(load_bits(qrow, K.id[w][i]));
+    __syncwarp();
+    for (int i0 = 0; i0 < nc; i0 += 32) {
+      const int i = i0 + lane;
+      float x = 0.f;
+      int j = 0;
+      if (i < nc) {
+        j = K.id[w][i];
+        const float v = K.v[w][i];
+        const bool kp = v > pr.thr || (v == pr.thr && j <= pr.tie);
+        x = kp ? ex2(fmaf(v, pr.c, -pr.bias)) : 0.f;
+        if (residual && x > 0.f) {
+          const float vq = K.r[w][i];
+          const bool kq = vq > qr.thr || (vq == qr.thr && j <= qr.tie);
+          if (kq) x = fmaxf(x - ex2(fmaf(vq, qr.c, -qr.bias)), 0.f);
+        }
+      }
+      float incl = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (i < nc) { K.r[w][i] = x; K.pre[w][i] = run + (incl - x); }
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+  }
+  if (lane == 0) K.wsum[w] = run;
+  g.sync();
+  if (t == 0) {
+    float s = 0.f;
+    for (int i = 0; i < kWarps; ++i) { K.wbase[i] = s; s += K.wsum[i]; }
+    sm.cta_sum = s;
+    sm.cta_ovf = K.cta_ovf;
+  }
+  cluster.sync();
+  float W = 0.f, acc = 0.f, cbase = 0.f;
+  int owner = -1, lastr = -1;
+  for (unsigned r = 0; r < C; ++r) {
+    bad |= *cluster.map_shared_rank(&sm.cta_ovf, r) != 0;
+    const float sr = *cluster.map_shared_rank(&sm.cta_sum, r);
+    if (sr > 0.f) lastr = (int)r;
+    W += sr;
+  }
+  const float target = (float)(u1 * (double)W);
+  for (unsigned r = 0; r < C; ++r) {
+    const float sr = *cluster.map_shared_rank(&sm.cta_sum, r);
+    if (sr > 0.f && acc <= target) { owner = (int)r; cbase = acc; }
+    acc += sr;
+  }
+  cluster.sync();  // every CTA has read the slice totals
+  if (bad) return __int_as_float(0x7FC00000);
+  if (!(W > 0.f)) return W;
+  if (owner < 0) { owner = lastr; cbase = 0.f; }
+  if (owner != (int)rank) return W;
+  // the owner: the last candidate with weight whose interval starts at or below the target
+  // (a target past every interval, from rounding, takes the last token with weight)
+  int best = -1;
+  for (int i = lane; i < nc; i += 32) {
+    const float x = K.r[w][i];
+    if (x > 0.f && cbase + K.wbase[w] + K.pre[w][i] <= target) best = i;
+  }
+  const int wb = __reduce_max_sync(0xFFFFFFFFu, (unsigned)(best + 1)) - 1;
+  int anyw = -1;
+  for (int i = lane; i < nc; i += 32) if (K.r[w][i] > 0.f) anyw = i;
+  const int wl = __reduce_max_sync(0xFFFFFFFFu, (unsigned)(anyw + 1)) - 1;
+  if (lane == 0) { K.best[w] = wb; K.last[w] = wl; }
+  g.sync();
+  if (t == 0) {
+    int tok = -1;
+    for (int i = kWarps - 1; i >= 0 && tok < 0; --i)
+      if (K.best[i] >= 0) tok = K.id[i][K.best[i]];
+    if (tok < 0)
+      for (int i = kWarps - 1; i >= 0 && tok < 0; --i)
+        if (K.last[i] >= 0) tok = K.id[i][K.last[i]];
+    *out = tok;
+  }
+  return W;
+}
+
 // Rule 2's draw for session b whose first rejection is a (a == M: the bonus from p_M).
 template <typename T>
 __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const Group& g, SessSmem& sm,
@@ -912,10 +1165,13 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
     const int np_cut = sp.thr_n, nq_cut = residual ? sq.thr_n : INT_MAX;
     const bool ties = np_cut != INT_MAX || nq_cut != INT_MAX;
     float W = __int_as_float(0x7FC00000);
-    // first choice: stream the slice through shared memory (the same decision in every CTA)
+    // first choice where p has a cut and the slices are short: weigh p's kept tokens only
+    if (filt_p && (long long)((V + (int)C - 1) / (int)C) * (long long)sizeof(T) <= kKeptSliceBytes)
+      W = draw_kept<T>(cluster, g, sm, trow, drow, residual, al_p, al_q, V, pr, qr, np_cut, nq_cut, u1, out);
+    // else stream the slice through shared memory (the same decision in every CTA)
     bool ok_all = true;
     for (unsigned r = 0; r < C; ++r) ok_all = ok_all && stream_ok<T>(V, C, r, al_p && (al_q || !residual), ties);
-    if (attempt == 0 && ok_all) {
+    if (W != W && attempt == 0 && ok_all) {
       if (ties) W = draw_stream<T, true, true>(cluster, g, sm, ring, trow, drow, residual, V, pr, qr, np_cut, nq_cut, u1, out);
       else if (filt) W = draw_stream<T, true, false>(cluster, g, sm, ring, trow, drow, residual, V, pr, qr, np_cut, nq_cut, u1, out);
       else W = draw_stream<T, false, false>(cluster, g, sm, ring, trow, drow, residual, V, pr, qr, np_cut, nq_cut, u1, out);
