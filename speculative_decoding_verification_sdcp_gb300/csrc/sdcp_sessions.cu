@@ -63,6 +63,8 @@ int launch_sessions(const SessIO& a, int dtype, bool pdl, cudaStream_t stream) {
   const void* fn = (dtype == SDCP_BF16) ? (const void*)session_kernel<__nv_bfloat16>
                                         : (const void*)session_kernel<float>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingBytes);
+  // all of the unified L1/shared storage as shared memory, so two CTAs fit on an SM
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return (int)e;
   if (dtype == SDCP_BF16)
     e = cudaLaunchKernelEx(&cfg, session_kernel<__nv_bfloat16>, a);
