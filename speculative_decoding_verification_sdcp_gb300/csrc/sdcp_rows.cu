@@ -16,7 +16,8 @@
 // Top-k / top-p on bf16 rows: all tokens that share a bf16 value have the same
 // probability, so the exact count of every value in a window below the row maximum decides
 // both cuts (the mass of a value is count * exp(v - max)).  The window (8 nats below the
-// maximum of the row's first stage) is counted while the row streams, with a shared-memory
+// maximum of the row's first stage; for top-k, down to a bound on the k-th largest token
+// from the first stage's thread maxima) is counted while the row streams, with a shared-memory
 // histogram of up to 2048 values: the stage loop marks the vectors whose maximum reaches
 // the window, each warp lists its marked vectors and counts them one vector per lane with
 // full-warp reductions; one warp then scans the bins for the k-th token and the top-p
@@ -72,6 +73,7 @@ struct RowShared {
   uint32_t r_thr_key;
   int r_kept, r_done, r_fallback;
   uint32_t hist[kWindowBins];
+  uint32_t kbins[32];     // thread maxima of the first stage by depth below its maximum (top-k)
   uint32_t hist_pad[32];  // one word per lane: where a lane with nothing to count adds 0
   uint16_t hits[kConsWarps][kVecPerThread * 32];  // per warp: stage vectors that reach the window
 };
@@ -995,8 +997,10 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       const RowCtx& x = plan.x;
       const T* row = row_ptr<T>(A, plan.row_id);
       const RowLayout L = row_layout(row, A.io.V);
-      if (x.window)  // fresh window for this row (ordered before use by the anchor's barriers)
+      if (x.window) {  // fresh window for this row (ordered before use by the anchor's barriers)
         for (int i = t; i < kWindowBins; i += kCons) sh.hist[i] = 0u;
+        if (t < 32) sh.kbins[t] = 0u;
+      }
       // the draft token's logit, loaded while the first stage is reduced
       const bool want_x = x.has_x && plan.xt >= 0 && (int64_t)plan.xt < A.io.V;
       uint32_t xbits = 0u;
@@ -1029,7 +1033,25 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
           float m0 = -INFINITY;
           for (int i = 0; i < kConsWarps; ++i) m0 = fmax_nan(m0, sh.w_m0[i]);
           const float dz = 8.f;
-          const float lo = m0 - dz * x.inv_scale;
+          float lo = m0 - dz * x.inv_scale;
+          if (x.topk && x.top_k <= (uint32_t)kCons && m0 == m0 && m0 > -INFINITY && m0 < INFINITY) {
+            // top-k: the thread maxima of this stage are maxima of disjoint sets of tokens, so
+            // if k of them are >= b, the row's k-th largest token is >= b.  b from a histogram
+            // of their depths below m0, in half units of log2 (32 bins): the window then holds
+            // the top-k cut, whatever the row's shape
+            const float dd = (m0 - acc.fm) * x.c;
+            atomicAdd(&sh.kbins[(dd >= 0.f && dd < 15.5f) ? (int)(dd * 2.f) : 31], 1u);
+            g.sync();
+            uint32_t cum = sh.kbins[l];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+              if (l >= o) cum += v;
+            }
+            const unsigned km = __ballot_sync(0xFFFFFFFFu, cum >= x.top_k);
+            const int kb = km ? __ffs(km) - 1 : 32;
+            if (kb < 31) lo = m0 - (float)(kb + 1) * 0.5f / x.c;  // one bf16 step of margin below
+          }
           w_on = (m0 == m0 && m0 > -INFINITY && m0 < INFINITY && lo > -3.0e38f) ? 1 : 0;
           if (w_on) {
             uint32_t lo16 = order_key(__float_as_uint(lo)) >> 16;
