@@ -30,15 +30,15 @@ template __global__ void session_kernel<float>(SessIO);
 template __global__ void session_kernel<__nv_bfloat16>(SessIO);
 
 // CTAs per session: as many as fit two CTAs per SM over the whole batch (a draw is a
-// latency-bound chain, so small batches gain from splitting it), never slices under 32
-// segments (8192 ids) of a row; 1 .. 8.
+// latency-bound chain, so small batches gain from splitting it), never slices under 16
+// segments (4096 ids) of a row; 1 .. 8.
 static int session_cluster(int64_t V, int32_t B) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 148;
   int64_t c = (2 * (int64_t)sms) / (B > 0 ? B : 1);
-  const int64_t by_size = V / 8192;
+  const int64_t by_size = V / 4096;
   if (c > by_size) c = by_size;
   return (int)(c < 1 ? 1 : (c > 8 ? 8 : c));
 }
