@@ -64,6 +64,8 @@ CASES = [
     (synth.F32, 50257, 3, "alternate", 1700, 0, 1000, 3.0, 1.0),
     (synth.BF16, 65536, 3, "spec", 900, 0, 1, 3.0, 1.0),           # top-p keeps only the argmax
     (synth.BF16, 65536, 3, "spec", 900, 0, 999, 3.0, 1.0),
+    (synth.BF16, 32000, 6, "spec", 800, 1000, 1000, 3.0, 1.0),     # top-k above 256: 8-nat window
+    (synth.BF16, 32000, 6, "spec", 800, 256, 950, 3.0, 1.0),       # top-k bound at k = 256, top-p
 ]
 
 
