@@ -481,9 +481,17 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
   auto e_of = [&](int d) { return ex2((key_value((top16 - (uint32_t)d) << 16) - lmax) * x.c); };
   long long cnt = 0;
   float mass = 0.f;
-  for (int d = d0; d < d1; ++d) {
-    const uint32_t c = hist[d];
-    if (c != 0u) { cnt += c; mass += (float)c * e_of(d); }
+  for (int d = d0; d < d1; d += 4) {  // four bins at a time (the loads and exps overlap)
+    uint32_t c[4];
+    float e[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      c[u] = (d + u < d1) ? hist[d + u] : 0u;
+      e[u] = e_of(d + u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (c[u] != 0u) { cnt += c[u]; mass += (float)c[u] * e[u]; }
   }
   // exclusive prefixes over the lanes (bins before the lane's first)
   long long ci = cnt;
@@ -530,22 +538,33 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
     long long ccb = 0;
     float cum = mpre;
     long long cc = cpre;
-    for (int d = d0; d < d1 && d <= dk; ++d) {
-      const uint32_t c = hist[d];
-      if (c == 0u) continue;
-      const float e = e_of(d);
-      const long long avail = (x.topk && d == dk) ? tk : (long long)c;
-      const float md = (float)avail * e;
-      const float nxt = cum + md;
-      if (md > 0.f && nxt >= target) {
-        long long n = (long long)ceilf(__fdiv_rn(target - cum, e));
-        if (n < 1) n = 1;
-        if (n > avail) n = avail;
-        cd = d; cn = (int)n; cb = cum; ccb = cc;
-        break;
+    const int dend = min(d1, dk + 1);
+    for (int d = d0; d < dend && cd < 0; d += 4) {  // four bins at a time, then in order
+      uint32_t c4[4];
+      float e4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        c4[u] = (d + u < dend) ? hist[d + u] : 0u;
+        e4[u] = e_of(d + u);
       }
-      cum = nxt;
-      cc += c;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t c = c4[u];
+        if (cd >= 0 || c == 0u) continue;
+        const float e = e4[u];
+        const long long avail = (x.topk && d + u == dk) ? tk : (long long)c;
+        const float md = (float)avail * e;
+        const float nxt = cum + md;
+        if (md > 0.f && nxt >= target) {
+          long long n = (long long)ceilf(__fdiv_rn(target - cum, e));
+          if (n < 1) n = 1;
+          if (n > avail) n = avail;
+          cd = d + u; cn = (int)n; cb = cum; ccb = cc;
+          continue;
+        }
+        cum = nxt;
+        cc += c;
+      }
     }
     const unsigned m = __ballot_sync(0xFFFFFFFFu, cd >= 0);
     if (m != 0u) {
