@@ -170,13 +170,6 @@ __device__ __forceinline__ uint32_t load_bits(const T* row, int64_t j) {
   return Elem<T>::bits(row[j]);
 }
 
-// Streaming 16-byte load that does not allocate in L1.
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
 
 // A row split into: head (scalar elements up to the first 16-byte boundary), nvec full
 // 16-byte vectors, and a scalar tail.
@@ -204,16 +197,6 @@ template <typename F>
 __device__ __forceinline__ float warp_reduce(float v, F op) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  return v;
-}
-__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  return v;
-}
-__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
 }
 __device__ __forceinline__ int64_t warp_max_i64(int64_t v) {
@@ -329,10 +312,6 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, co
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
-// Named barrier for a subset of the block (thread count a multiple of 32).
-__device__ __forceinline__ void named_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 // Named barrier 1 (the id is a literal, so a kernel reserves no other barrier for it).
 __device__ __forceinline__ void named_sync1(int nthreads) {
