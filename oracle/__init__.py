@@ -80,6 +80,11 @@ def lib():
         L.oracle_verify_batch.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp,
                                           vp, vp, vp, vp, vp, ctypes.c_int]
         L.oracle_verify_batch.restype = ctypes.c_int
+        L.oracle_row_stats_batch.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, vp,
+                                             vp, ctypes.c_int]
+        L.oracle_row_stats_batch.restype = ctypes.c_int
+        L.oracle_set_topp_shift.argtypes = [ctypes.c_double]
+        L.oracle_set_topp_shift.restype = None
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = ctypes.c_int
         _lib = L
@@ -172,6 +177,54 @@ def verify_batch(target: np.ndarray, draft: np.ndarray | None, m_offsets: np.nda
     if rc != 0:
         raise ValueError("oracle_verify_batch rejected its arguments (rc=%d)" % rc)
     return {"accepted": acc, "n_out": nout, "out_tokens": toks, "status": st, "detail": det}
+
+
+ROW_INFO_DTYPE = np.dtype([("lmax", "<f8"), ("log_s", "<f8"), ("argmax", "<i4"), ("kept", "<i4"),
+                           ("k1", "<i4"), ("invalid", "<i4"), ("topp_cum_before", "<f8"),
+                           ("topp_cum_at", "<f8"), ("topp_target", "<f8")])
+assert ROW_INFO_DTYPE.itemsize == ctypes.sizeof(RowInfo)
+
+
+def row_stats_batch(target: np.ndarray, draft: np.ndarray, m_offsets: np.ndarray,
+                    draft_tokens: np.ndarray, params: np.ndarray, nthreads: int = 1):
+    """The sampling profile (SDCP Section 4.1) of every scored row of a ragged batch, in the
+    row order of the C ABI's row-statistics call (target rows, then draft rows).
+
+    Returns (info [R] ROW_INFO_DTYPE, lpx [R] float64, skipped [R] bool)."""
+    target = np.ascontiguousarray(target)
+    draft = np.ascontiguousarray(draft)
+    dcode = _dtype_code(target)
+    m_offsets = np.ascontiguousarray(m_offsets, dtype=np.int32)
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    params = np.ascontiguousarray(params, dtype=PARAMS_DTYPE)
+    B = params.shape[0]
+    total = int(draft_tokens.shape[0])
+    R = 2 * total + B
+    info = np.zeros(R, ROW_INFO_DTYPE)
+    lpx = np.zeros(R, np.float64)
+    skipped = np.zeros(R, np.int32)
+    rc = lib().oracle_row_stats_batch(_ptr(target), _ptr(draft), dcode, target.shape[1], B,
+                                      _ptr(m_offsets), total, _ptr(draft_tokens), _ptr(params),
+                                      _ptr(info), _ptr(lpx), _ptr(skipped), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_row_stats_batch rejected its arguments (rc=%d)" % rc)
+    return info, lpx, skipped.astype(bool)
+
+
+class topp_shift:
+    """Context manager: the oracle's top-p target times (1 + rel) inside the block (the two
+    readings of a top-p crossing that lies within rounding of P)."""
+
+    def __init__(self, rel: float):
+        self.rel = float(rel)
+
+    def __enter__(self):
+        lib().oracle_set_topp_shift(self.rel)
+        return self
+
+    def __exit__(self, *exc):
+        lib().oracle_set_topp_shift(0.0)
+        return False
 
 
 def max_threads() -> int:

@@ -137,6 +137,15 @@ static double logit_at(const void* row, int dtype, int64_t j) {
   return (double)f;
 }
 
+/*
+ * Relative shift of the top-p target, 0 by default.  The top-p crossing is a decision
+ * boundary: where the cumulative mass lies within rounding of P, keeping the crossing
+ * token and leaving it out are both faithful to Section 4.1.  The parity tests set a shift
+ * of -1e-5 or +1e-5 to form the two readings of such a row; nothing else changes it.
+ */
+static double g_topp_shift = 0.0;
+void oracle_set_topp_shift(double rel) { g_topp_shift = rel; }
+
 /* Sort support: ids ordered by (logit descending, id ascending). */
 typedef struct { double l; int32_t id; } orc_pair;
 static int cmp_desc(const void* a, const void* b) {
@@ -211,7 +220,7 @@ int oracle_row_dist(const void* row, int dtype, int64_t V, uint32_t temperature_
   /* top-p: minimal prefix of the same order whose cumulative probability >= P. */
   int64_t k2 = k1;
   if (filter_p) {
-    double target = (double)top_p_milli / 1000.0;
+    double target = (double)top_p_milli / 1000.0 * (1.0 + g_topp_shift);
     double cum = 0.0, before = 0.0;
     k2 = k1;
     for (int64_t r = 0; r < k1; ++r) {
@@ -236,6 +245,72 @@ int oracle_row_dist(const void* row, int dtype, int64_t V, uint32_t temperature_
   }
   free(pi);
   free(ord);
+  return 0;
+}
+
+/*
+ * Statistics of every scored row of a ragged batch, in the row order of the C ABI's
+ * row-statistics call: the total + B target rows, then the total draft rows.  Each row is
+ * formed by oracle_row_dist under its session's profile; lpx[r] is the natural log of the
+ * row's probability of its draft token (target row i < M and draft row i carry x[i]):
+ * -inf outside the kept set, NaN for a row without a token or with one outside [0, V).
+ * skipped[r] = 1 for rows of sessions whose offsets or top_p_milli make no distribution.
+ * Rows are independent; nthreads > 1 forms them on OpenMP threads.
+ */
+int oracle_row_stats_batch(const void* T, const void* D, int dtype, int64_t V, int32_t B,
+                           const int32_t* m_offsets, int64_t total, const int32_t* x,
+                           const orc_params* params, orc_row_info* info, double* lpx,
+                           int32_t* skipped, int nthreads) {
+  if (B < 0 || V < 1 || total < 0 || (dtype != ORC_F32 && dtype != ORC_BF16)) return 1;
+  const int64_t R_T = total + B, R = R_T + total;
+  size_t esz = (dtype == ORC_F32) ? 4 : 2;
+  /* session and draft token of every row */
+  int32_t* sess = (int32_t*)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+  int32_t* tok = (int32_t*)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+  for (int64_t r = 0; r < R; ++r) { sess[r] = -1; tok[r] = -1; }
+  for (int32_t b = 0; b < B; ++b) {
+    int64_t o0 = m_offsets[b], o1 = m_offsets[b + 1];
+    if (o0 < 0 || o1 < o0 || o1 > total) continue;
+    for (int64_t i = 0; i <= o1 - o0; ++i) {
+      sess[o0 + b + i] = b;
+      tok[o0 + b + i] = (i < o1 - o0) ? 1 : 0;
+    }
+    for (int64_t i = 0; i < o1 - o0; ++i) { sess[R_T + o0 + i] = b; tok[R_T + o0 + i] = 1; }
+  }
+#ifdef _OPENMP
+  if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+#endif
+  {
+    double* dist = (double*)malloc(sizeof(double) * (size_t)V);
+    uint8_t* kept = (uint8_t*)malloc((size_t)V);
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (int64_t r = 0; r < R; ++r) {
+      memset(&info[r], 0, sizeof info[r]);
+      lpx[r] = NAN;
+      const int32_t b = sess[r];
+      if (b < 0 || params[b].top_p_milli > 1000) { skipped[r] = 1; continue; }
+      skipped[r] = 0;
+      const int is_target = r < R_T;
+      const char* row = is_target ? (const char*)T + (size_t)r * (size_t)V * esz
+                                  : (const char*)D + (size_t)(r - R_T) * (size_t)V * esz;
+      const orc_params* p = &params[b];
+      if (oracle_row_dist(row, dtype, V, p->temperature_milli, p->top_k, p->top_p_milli, dist,
+                          kept, &info[r]))
+        continue;
+      if (tok[r] == 1) {
+        const int64_t xi = is_target ? (int64_t)x[r - b] : (int64_t)x[r - R_T];
+        if (xi >= 0 && xi < V)
+          lpx[r] = (kept[xi] && dist[xi] > 0.0) ? log(dist[xi]) : -INFINITY;
+      }
+    }
+    free(dist);
+    free(kept);
+  }
+  free(sess);
+  free(tok);
   return 0;
 }
 

@@ -100,6 +100,22 @@ def test_philox_matches_library_implementation(oracle_mod):
         assert [int(x) for x in oracle_mod.philox4x32_10(ctr, key)] == r
 
 
+def test_uniform_is_first_53_bits_of_the_output(oracle_mod):
+    """u = the first 53 bits of the generator's output / 2^53, read straight from the
+    published known-answer outputs as text: the hex digits of words 0 and 1, in that order,
+    form one 64-bit number whose top 53 bits are u * 2^53.  Counter words are (position,
+    purpose, round, session tag), key words the low and high halves of the seed."""
+    kat = json.load(open(golden_path("philox4x32_10_kat.json")))
+    for v in kat["vectors"]:
+        ctr = [int(h, 16) for h in v["counter"]]
+        key = [int(h, 16) for h in v["key"]]
+        top64 = int(v["out"][0] + v["out"][1], 16)
+        expect = (top64 >> 11) / float(2 ** 53)
+        seed = key[0] | (key[1] << 32)
+        got = oracle_mod.uniform(seed, ctr[2], ctr[0], ctr[1], ctr[3])
+        assert got == expect, (v, got, expect)
+
+
 def test_uniform_range_and_uniformity(oracle_mod):
     """u in [0, 1), chi-square on 64 equal bins over 2^17 counters."""
     n = 1 << 17
@@ -495,3 +511,44 @@ def test_reproducible(oracle_mod):
     r2 = oracle_mod.verify_batch(target, draft, off, toks, prm, nthreads=4)
     for key in ("accepted", "n_out", "out_tokens", "status"):
         assert (r1[key] == r2[key]).all()
+
+
+def test_row_stats_batch_row_order_and_tokens(oracle_mod):
+    """The batch helper of the parity tests visits rows in the C ABI's row-statistics order
+    (target rows, then draft rows) and reads each row's own draft token: checked row by row
+    against the single-row profile on a small ragged batch."""
+    rng = np.random.default_rng(3)
+    Ms = [1, 4, 2, 3]
+    B, V = len(Ms), 37
+    off = _offsets(Ms)
+    tot = int(off[-1])
+    T = (rng.normal(0, 2, size=(tot + B, V))).astype(np.float32)
+    D = (rng.normal(0, 2, size=(tot, V))).astype(np.float32)
+    x = rng.integers(0, V, size=tot).astype(np.int32)
+    x[2] = V + 3  # out of range: no probability
+    prm = _params(oracle_mod, B, T=800, k=9, p=900)
+    prm["temperature_milli"][1] = 0
+    info, lpx, skipped = oracle_mod.row_stats_batch(T, D, off, x, prm, nthreads=2)
+    assert not skipped.any()
+    r = 0
+    for b in range(B):
+        for i in range(Ms[b] + 1):
+            dist, kept, inf1, rc = oracle_mod.row_dist(T[r], int(prm["temperature_milli"][b]), 9, 900, want_kept=True)
+            assert info[r]["kept"] == inf1.kept and info[r]["log_s"] == inf1.log_s
+            if i < Ms[b]:
+                xi = int(x[off[b] + i])
+                if xi >= V:
+                    assert np.isnan(lpx[r])
+                else:
+                    assert lpx[r] == (np.log(dist[xi]) if kept[xi] else -np.inf)
+            else:
+                assert np.isnan(lpx[r])
+            r += 1
+    for d in range(tot):
+        b = int(np.searchsorted(off, d, side="right") - 1)
+        dist, kept, inf1, rc = oracle_mod.row_dist(D[d], int(prm["temperature_milli"][b]), 9, 900, want_kept=True)
+        assert info[r]["kept"] == inf1.kept
+        xi = int(x[d])
+        if xi < V:
+            assert lpx[r] == (np.log(dist[xi]) if kept[xi] else -np.inf)
+        r += 1
