@@ -240,6 +240,27 @@ int sdcp_verify_batch_noalloc(const void* target_logits, const void* draft_logit
                               int32_t* n_out, int32_t* out_tokens, int32_t* status,
                               void* stream);
 
+/*
+ * Host-side split of one ragged batch into n_parts contiguous blocks of sessions for
+ * n_parts GPUs (one process per GPU).  Sessions are independent (Section 6.3 "Scoring":
+ * a verifier may batch the proposals of many sessions), so block k can be verified on its
+ * own GPU, and concatenating the blocks' outputs in order gives the whole batch's outputs:
+ * no collective is needed on the data path.
+ *
+ * m_offsets  host, [B+1] int32 (as for sdcp_verify_batch).
+ * params     host, [B] sdcp_session_params, or NULL (every session counted as Rule 2).
+ * bounds     host out, [n_parts+1] int32: block k holds sessions bounds[k] .. bounds[k+1]-1;
+ *            bounds[0] = 0, bounds[n_parts] = B, non-decreasing.
+ * The blocks are balanced by the rows each session makes the first phase read: M_b + 1
+ * target rows, plus M_b draft rows under Rule 2.  Boundary k is the first session index
+ * (not before boundary k-1) whose prefix of rows comes closest to k/n_parts of the total;
+ * the split is a pure function of its inputs.
+ * Returns SDCP_OK, or SDCP_E_INVALID for null pointers, B < 0, n_parts < 1 or offsets that
+ * are not non-decreasing from 0.  Touches no device.
+ */
+int sdcp_split_sessions(const int32_t* m_offsets, const sdcp_session_params* params, int32_t B,
+                        int32_t n_parts, int32_t* bounds);
+
 /* Human-readable text for an SDCP_E_* code (static storage, never NULL). */
 const char* sdcp_strerror(int code);
 

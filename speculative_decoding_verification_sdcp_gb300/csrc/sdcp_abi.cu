@@ -3,16 +3,17 @@
 // workspace header, the row kernel, then the session kernel (a programmatic dependent of
 // the row kernel in sdcp_verify_batch).
 #include <climits>
+#include <vector>
 
 #include "sdcp_device.cuh"
 
 namespace sdcp {
 
-
 namespace {
-
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+}  // namespace
 
+// Host-side checks every verify entry point runs first, in this order.
 int check_common(const void* target, int dtype, int64_t V, int32_t B, const int32_t* m_offsets,
                  int64_t total, const int32_t* tokens, const sdcp_session_params* params,
                  const void* draft) {
@@ -27,8 +28,8 @@ int check_common(const void* target, int dtype, int64_t V, int32_t B, const int3
   return SDCP_OK;
 }
 
+namespace {
 int check_workspace(void* workspace, size_t workspace_bytes, int64_t V, int32_t B, int64_t total);
-
 }  // namespace
 }  // namespace sdcp
 
@@ -167,6 +168,40 @@ int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtyp
   const SessIO io = make_io(target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens,
                             params, nullptr, nullptr, nullptr, nullptr, workspace);
   return launch_rows(io, workspace, stats_out, 1, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sdcp_split_sessions(const int32_t* m_offsets, const sdcp_session_params* params, int32_t B,
+                        int32_t n_parts, int32_t* bounds) {
+  if (!m_offsets || !bounds || B < 0 || n_parts < 1) return SDCP_E_INVALID;
+  if (m_offsets[0] != 0) return SDCP_E_INVALID;
+  for (int32_t b = 0; b < B; ++b)
+    if (m_offsets[b + 1] < m_offsets[b]) return SDCP_E_INVALID;
+  // prefix of scored rows: M_b + 1 target rows, plus M_b draft rows under Rule 2
+  std::vector<int64_t> pre((size_t)B + 1, 0);
+  for (int32_t b = 0; b < B; ++b) {
+    const int64_t M = (int64_t)m_offsets[b + 1] - m_offsets[b];
+    const bool rule2 = !params || params[b].rule_id == SDCP_RULE_SPECULATIVE_SAMPLING;
+    pre[(size_t)b + 1] = pre[(size_t)b] + M + 1 + (rule2 ? M : 0);
+  }
+  const int64_t total = pre[(size_t)B];
+  bounds[0] = 0;
+  int32_t cut = 0;
+  for (int32_t k = 1; k < n_parts; ++k) {
+    // target k * total / n_parts, compared as k * total vs pre * n_parts (exact in int64)
+    const int64_t goal = (int64_t)k * total;
+    int32_t best = cut;
+    int64_t best_d = INT64_MAX;
+    for (int32_t b = cut; b <= B; ++b) {
+      const int64_t d = pre[(size_t)b] * n_parts - goal;
+      const int64_t ad = d < 0 ? -d : d;
+      if (ad < best_d) { best_d = ad; best = b; }
+      if (d >= 0) break;  // the prefix only grows from here
+    }
+    cut = best;
+    bounds[k] = cut;
+  }
+  bounds[n_parts] = B;
+  return SDCP_OK;
 }
 
 }  // extern "C"

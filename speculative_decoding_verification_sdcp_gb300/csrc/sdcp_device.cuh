@@ -70,6 +70,17 @@ struct RowArgs {
 };
 
 int launch_row_stats(const RowArgs& a, int dtype, cudaStream_t stream);
+int check_common(const void* target, int dtype, int64_t V, int32_t B, const int32_t* m_offsets,
+                 int64_t total, const int32_t* tokens, const sdcp_session_params* params,
+                 const void* draft);
+
+// Device facts the launches need, looked up once per device (the SM count, and the
+// kernels' shared-memory attributes set once).  Returns false if the device query failed.
+struct DeviceInfo {
+  int sms;
+  int row_ctas_per_sm;
+};
+bool device_info(DeviceInfo* out);
 int launch_sessions(const SessIO& a, int dtype, bool pdl, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------------
@@ -263,12 +274,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
                : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
   return done != 0;
-}
-// Bounded wait for the phase of `parity` to complete: false after `limit` polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit) {
-  for (long long it = 0; it < limit; ++it)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
 }
 // Nanoseconds of the GPU's global timer.
 __device__ __forceinline__ unsigned long long global_ns() {

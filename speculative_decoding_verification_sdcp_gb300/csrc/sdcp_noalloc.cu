@@ -43,13 +43,15 @@ extern "C" int sdcp_verify_batch_noalloc(const void* target_logits, const void* 
                                          const sdcp_session_params* params, int32_t* accepted,
                                          int32_t* n_out, int32_t* out_tokens, int32_t* status,
                                          void* stream) {
-  if (B < 0 || total_drafts < 0 || V < 1) return SDCP_E_INVALID;
+  int rc = sdcp::check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens,
+                              params, draft_logits);
+  if (rc != SDCP_OK) return rc;
   if (B == 0) return SDCP_OK;
   const size_t need = sdcp_workspace_bytes(V, B, total_drafts);
   if (need == 0) return V > SDCP_MAX_VOCAB ? SDCP_E_TOO_LARGE : SDCP_E_INVALID;
   if (need > SDCP_NOALLOC_SCRATCH_BYTES) return SDCP_E_SCRATCH_LIMIT;
   void* scratch = nullptr;
-  int rc = scratch_for_current_device(&scratch);
+  rc = scratch_for_current_device(&scratch);
   if (rc != SDCP_OK) return rc;
   return sdcp_verify_batch(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
                            draft_tokens, params, accepted, n_out, out_tokens, status, scratch,

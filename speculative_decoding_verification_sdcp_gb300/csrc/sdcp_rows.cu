@@ -25,6 +25,7 @@
 // their number is recorded.  Rows the window cannot decide are searched again from L2
 // (wider windows, then a bisection over the order-key space).
 #include <climits>
+#include <mutex>
 
 #include "sdcp_session.cuh"
 
@@ -936,6 +937,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    uint32_t issued = 0u, issued_par = 0u;  // lane 0: stages with a copy issued, and its parity
     auto fetch = [&]() -> long long {
       unsigned long long r = 0;
       if (l == 0) r = atomicAdd(&A.hdr->next_slot, 1ull);
@@ -970,6 +972,8 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
             if (c == 0) sh.plan[stage] = RowPlan{cur.row_id, nch, cur.xt, cur.x};
             mbar_arrive_expect_tx(&sh.full[stage], bytes);
             if (bytes > 0) bulk_copy_g2s(ring + (size_t)stage * kChunk, src + off, bytes, &sh.full[stage]);
+            issued |= 1u << stage;
+            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           }
         }
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
@@ -992,11 +996,11 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       } else {
         sh.abort = 1;
         atomicOr(&A.hdr->error, 1u);
-        // let copies already issued land before the CTA can exit (bounded)
-        for (int s = 0; s < kStages; ++s) {
-          (void)mbar_wait(&sh.full[s], 0, 1 << 12);
-          (void)mbar_wait(&sh.full[s], 1, 1 << 12);
-        }
+        // before the CTA may exit, the last copy issued into each stage must have landed
+        // (at most one per stage is outstanding: a stage is refilled only after its last
+        // copy was consumed); each wait is bounded by wall time
+        for (int s = 0; s < kStages; ++s)
+          if ((issued >> s) & 1u) (void)mbar_wait_for(&sh.full[s], (issued_par >> s) & 1u, nullptr);
       }
     }
     return;
@@ -1103,30 +1107,59 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
 template __global__ void row_stats_kernel<float>(RowArgs);
 template __global__ void row_stats_kernel<__nv_bfloat16>(RowArgs);
 
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr size_t kRingBytes = (size_t)kStages * kChunk;
+struct DeviceCache {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  DeviceInfo info{0, 0};
+};
+DeviceCache g_device_cache[kMaxDevices];
+
+// Once per device (with that device current): the SM count, the row kernels' shared-memory
+// attributes (all of the unified L1/shared storage as shared memory, so two CTAs fit on an
+// SM) and their occupancy.  A launch then costs no attribute or occupancy query.
+cudaError_t setup_device(int dev, DeviceInfo* info) {
+  int sms = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && sms <= 0) e = cudaErrorInvalidDevice;
+  int per_sm = kRowCtasPerSm;
+  const void* fns[2] = {(const void*)row_stats_kernel<__nv_bfloat16>, (const void*)row_stats_kernel<float>};
+  for (const void* fn : fns) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    int n = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kRowThreads, kRingBytes);
+    if (e == cudaSuccess) per_sm = min(per_sm, max(n, 1));
+  }
+  info->sms = sms;
+  info->row_ctas_per_sm = per_sm;
+  return e;
+}
+}  // namespace
+
+bool device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  DeviceCache& c = g_device_cache[dev];
+  std::call_once(c.once, [&] { c.err = setup_device(dev, &c.info); });
+  if (c.err != cudaSuccess) return false;
+  *out = c.info;
+  return true;
+}
+
 int launch_row_stats(const RowArgs& a, int dtype, cudaStream_t stream) {
   const long long rows = a.io.total + a.io.B + a.io.total;
   if (rows <= 0) return 0;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-    return (int)cudaErrorInvalidDevice;
-  const size_t ring_bytes = (size_t)kStages * kChunk;
-  const void* fn = (dtype == SDCP_BF16) ? (const void*)row_stats_kernel<__nv_bfloat16>
-                                        : (const void*)row_stats_kernel<float>;
-  // all of the unified L1/shared storage as shared memory, so two CTAs fit on an SM
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring_bytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e != cudaSuccess) return (int)e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRowThreads, ring_bytes);
-  if (e != cudaSuccess) return (int)e;
-  if (per_sm < 1) per_sm = 1;
-  const long long grid = min(rows, (long long)sms * min(per_sm, kRowCtasPerSm));
+  DeviceInfo di;
+  if (!device_info(&di)) return (int)cudaErrorInvalidDevice;
+  const long long grid = min(rows, (long long)di.sms * di.row_ctas_per_sm);
   if (dtype == SDCP_BF16)
-    row_stats_kernel<__nv_bfloat16><<<(unsigned)grid, kRowThreads, ring_bytes, stream>>>(a);
+    row_stats_kernel<__nv_bfloat16><<<(unsigned)grid, kRowThreads, kRingBytes, stream>>>(a);
   else
-    row_stats_kernel<float><<<(unsigned)grid, kRowThreads, ring_bytes, stream>>>(a);
-  e = cudaGetLastError();
+    row_stats_kernel<float><<<(unsigned)grid, kRowThreads, kRingBytes, stream>>>(a);
+  const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? 0 : (int)e;
 }
 

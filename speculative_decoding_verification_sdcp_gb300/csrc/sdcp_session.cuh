@@ -693,13 +693,16 @@ __device__ float draw_stream(cg::cluster_group& cluster, const Group& g, SessSme
   else if (t == 0) { sm.overflow = 0; sm.tie_p_cand = INT_MAX; sm.tie_q_cand = INT_MAX; }
   g.sync();  // every thread has read ring_uses
   bool fail = false;
+  int issued = 0;  // thread 0: stages whose copies were issued (always a prefix 0 .. issued-1)
   auto issue = [&](int s) {  // thread 0: stage s of the slice into its slot
     const uint32_t u = use0 + (uint32_t)s;
     const int slot = (int)(u % kDrawStages);
+    if (fail) return;
     if (u >= kDrawStages && !mbar_wait_for(&sm.empty[slot], ((u / kDrawStages) - 1) & 1u, nullptr)) {
       fail = true;
       return;
     }
+    issued = s + 1;
     const int n = min(S, hi - (lo + s * S));
     const uint32_t bytes = (uint32_t)n * sizeof(T);
     unsigned char* dst = ring + (size_t)slot * 2 * kDrawHalf;
@@ -778,10 +781,10 @@ __device__ float draw_stream(cg::cluster_group& cluster, const Group& g, SessSme
   }
   if (TIES && lane == 0) sm.tie_n[w] = nt;
   if (lane == 0 && (ovf || fail)) sm.overflow = 1;
-  if (t == 0 && fail) {  // a wait gave up: let the copies already issued land first (bounded)
-    for (int s = max(0, nst - kDrawStages); s < nst; ++s) {
+  if (t == 0 && fail) {  // a wait gave up: the copies already issued land first (bounded)
+    for (int s = max(0, issued - kDrawStages); s < issued; ++s) {
       const uint32_t u = use0 + (uint32_t)s;
-      (void)mbar_wait(&sm.full[u % kDrawStages], (u / kDrawStages) & 1u, 1 << 14);
+      (void)mbar_wait_for(&sm.full[u % kDrawStages], (u / kDrawStages) & 1u, nullptr);
     }
   }
   if (t == 0) sm.ring_uses = use0 + (uint32_t)nst;

@@ -4,6 +4,8 @@
 // sdcp_session.cuh on the row statistics phase 1 left in the workspace.  Launched as a
 // programmatic dependent of the row kernel, it waits for the row statistics before
 // reading them.
+#include <mutex>
+
 #include "sdcp_session.cuh"
 
 namespace sdcp {
@@ -32,20 +34,44 @@ template __global__ void session_kernel<__nv_bfloat16>(SessIO);
 // CTAs per session: as many as fit two CTAs per SM over the whole batch (a draw is a
 // latency-bound chain, so small batches gain from splitting it), never slices under 16
 // segments (4096 ids) of a row; 1 .. 8.
-static int session_cluster(int64_t V, int32_t B) {
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 148;
+static int session_cluster(int sms, int64_t V, int32_t B) {
   int64_t c = (2 * (int64_t)sms) / (B > 0 ? B : 1);
   const int64_t by_size = V / 4096;
   if (c > by_size) c = by_size;
   return (int)(c < 1 ? 1 : (c > 8 ? 8 : c));
 }
 
+namespace {
+constexpr int kMaxDevices = 64;
+std::once_flag g_once[kMaxDevices];
+cudaError_t g_err[kMaxDevices];
+
+// Once per device: the session kernels' shared-memory attributes (the draw ring as dynamic
+// shared memory, and all of the unified L1/shared storage as shared memory, so two CTAs fit
+// on an SM).
+cudaError_t session_attributes(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_once[dev], [&] {
+    cudaError_t e = cudaSuccess;
+    const void* fns[2] = {(const void*)session_kernel<__nv_bfloat16>, (const void*)session_kernel<float>};
+    for (const void* fn : fns) {
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingBytes);
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    }
+    g_err[dev] = e;
+  });
+  return g_err[dev];
+}
+}  // namespace
+
 int launch_sessions(const SessIO& a, int dtype, bool pdl, cudaStream_t stream) {
   if (a.B <= 0) return 0;
-  const int C = session_cluster(a.V, a.B);
+  DeviceInfo di;
+  int dev = 0;
+  if (!device_info(&di) || cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
+  cudaError_t e = session_attributes(dev);
+  if (e != cudaSuccess) return (int)e;
+  const int C = session_cluster(di.sms, a.V, a.B);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((int64_t)a.B * C), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -60,12 +86,6 @@ int launch_sessions(const SessIO& a, int dtype, bool pdl, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  const void* fn = (dtype == SDCP_BF16) ? (const void*)session_kernel<__nv_bfloat16>
-                                        : (const void*)session_kernel<float>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingBytes);
-  // all of the unified L1/shared storage as shared memory, so two CTAs fit on an SM
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e != cudaSuccess) return (int)e;
   if (dtype == SDCP_BF16)
     e = cudaLaunchKernelEx(&cfg, session_kernel<__nv_bfloat16>, a);
   else

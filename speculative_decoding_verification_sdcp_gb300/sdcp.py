@@ -55,6 +55,8 @@ def _load():
     L.sdcp_verify_batch_noalloc.restype = ctypes.c_int
     L.sdcp_row_stats.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, vp, sz, vp]
     L.sdcp_row_stats.restype = ctypes.c_int
+    L.sdcp_split_sessions.argtypes = [vp, vp, i32, i32, vp]
+    L.sdcp_split_sessions.restype = ctypes.c_int
     L.sdcp_strerror.argtypes = [ctypes.c_int]
     L.sdcp_strerror.restype = ctypes.c_char_p
     L.sdcp_abi_version.argtypes = []
@@ -111,6 +113,11 @@ def _stream_handle(device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def _on(t: torch.Tensor):
+    """The library launches on the current CUDA device: make the tensors' device current."""
+    return torch.cuda.device(t.device)
+
+
 def sdcp_verify_batch(target_logits, draft_logits, m_offsets, total_drafts, draft_tokens,
                       params_dev, accepted, n_out, out_tokens, status, workspace,
                       stream=None):
@@ -118,10 +125,11 @@ def sdcp_verify_batch(target_logits, draft_logits, m_offsets, total_drafts, draf
     V = target_logits.shape[1]
     B = accepted.shape[0]
     s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
-    rc = lib.sdcp_verify_batch(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits),
-                               V, B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
-                               _ptr(params_dev), _ptr(accepted), _ptr(n_out), _ptr(out_tokens),
-                               _ptr(status), _ptr(workspace), workspace.numel(), s)
+    with _on(target_logits):
+        rc = lib.sdcp_verify_batch(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits),
+                                   V, B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
+                                   _ptr(params_dev), _ptr(accepted), _ptr(n_out), _ptr(out_tokens),
+                                   _ptr(status), _ptr(workspace), workspace.numel(), s)
     _check(rc, "sdcp_verify_batch")
 
 
@@ -135,10 +143,11 @@ def sdcp_verify_batch_noalloc(target_logits, draft_logits, m_offsets, total_draf
     V = target_logits.shape[1]
     B = accepted.shape[0]
     s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
-    rc = lib.sdcp_verify_batch_noalloc(_ptr(target_logits), _ptr(draft_logits),
-                                       dtype_code(target_logits), V, B, _ptr(m_offsets),
-                                       int(total_drafts), _ptr(draft_tokens), _ptr(params_dev),
-                                       _ptr(accepted), _ptr(n_out), _ptr(out_tokens), _ptr(status), s)
+    with _on(target_logits):
+        rc = lib.sdcp_verify_batch_noalloc(_ptr(target_logits), _ptr(draft_logits),
+                                           dtype_code(target_logits), V, B, _ptr(m_offsets),
+                                           int(total_drafts), _ptr(draft_tokens), _ptr(params_dev),
+                                           _ptr(accepted), _ptr(n_out), _ptr(out_tokens), _ptr(status), s)
     _check(rc, "sdcp_verify_batch_noalloc")
 
 
@@ -146,9 +155,10 @@ def sdcp_verify_rows(target_logits, draft_logits, m_offsets, total_drafts, draft
                      params_dev, workspace, B, stream=None):
     V = target_logits.shape[1]
     s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
-    rc = lib.sdcp_verify_rows(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits), V,
-                              B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
-                              _ptr(params_dev), _ptr(workspace), workspace.numel(), s)
+    with _on(target_logits):
+        rc = lib.sdcp_verify_rows(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits), V,
+                                  B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
+                                  _ptr(params_dev), _ptr(workspace), workspace.numel(), s)
     _check(rc, "sdcp_verify_rows")
 
 
@@ -157,10 +167,11 @@ def sdcp_verify_sessions(target_logits, draft_logits, m_offsets, total_drafts, d
     V = target_logits.shape[1]
     B = accepted.shape[0]
     s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
-    rc = lib.sdcp_verify_sessions(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits),
-                                  V, B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
-                                  _ptr(params_dev), _ptr(accepted), _ptr(n_out), _ptr(out_tokens),
-                                  _ptr(status), _ptr(workspace), workspace.numel(), s)
+    with _on(target_logits):
+        rc = lib.sdcp_verify_sessions(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits),
+                                      V, B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
+                                      _ptr(params_dev), _ptr(accepted), _ptr(n_out), _ptr(out_tokens),
+                                      _ptr(status), _ptr(workspace), workspace.numel(), s)
     _check(rc, "sdcp_verify_sessions")
 
 
@@ -169,10 +180,24 @@ def sdcp_row_stats(target_logits, draft_logits, m_offsets, total_drafts, draft_t
     V = target_logits.shape[1]
     B = m_offsets.shape[0] - 1
     s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
-    rc = lib.sdcp_row_stats(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits), V, B,
-                            _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens), _ptr(params_dev),
-                            _ptr(stats_out), _ptr(workspace), workspace.numel(), s)
+    with _on(target_logits):
+        rc = lib.sdcp_row_stats(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits), V, B,
+                                _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens), _ptr(params_dev),
+                                _ptr(stats_out), _ptr(workspace), workspace.numel(), s)
     _check(rc, "sdcp_row_stats")
+
+
+def sdcp_split_sessions(m_offsets: np.ndarray, params: np.ndarray | None, n_parts: int) -> np.ndarray:
+    """Contiguous session blocks for n_parts GPUs (host arrays in, [n_parts+1] bounds out)."""
+    off = np.ascontiguousarray(m_offsets, dtype=np.int32)
+    B = off.shape[0] - 1
+    prm = None if params is None else np.ascontiguousarray(params, dtype=PARAMS_DTYPE)
+    bounds = np.zeros(n_parts + 1, dtype=np.int32)
+    rc = lib.sdcp_split_sessions(off.ctypes.data_as(ctypes.c_void_p),
+                                 None if prm is None else prm.ctypes.data_as(ctypes.c_void_p),
+                                 B, int(n_parts), bounds.ctypes.data_as(ctypes.c_void_p))
+    _check(rc, "sdcp_split_sessions")
+    return bounds
 
 
 class Verifier:

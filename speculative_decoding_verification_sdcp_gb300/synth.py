@@ -225,6 +225,20 @@ def make_batch(w: Workload, device="cpu", max_sessions: int | None = None,
     return Batch(w, target, draft, m_off, tokens, params, params_to_device(params, dev))
 
 
+def shard_batch(batch: Batch, lo: int, hi: int) -> Batch:
+    """Sessions lo .. hi-1 of a batch as a batch of their own: views of the same row buffers
+    (the sessions' rows are contiguous in the ragged layout), offsets rebased to 0."""
+    offs = batch.m_offsets.detach().cpu().numpy().astype(np.int64)
+    o0, o1 = int(offs[lo]), int(offs[hi])
+    target = batch.target[o0 + lo:o1 + hi]
+    draft = batch.draft[o0:o1]
+    m_off = torch.from_numpy((offs[lo:hi + 1] - o0).astype(np.int32)).to(batch.target.device)
+    tokens = batch.draft_tokens[o0:o1]
+    params = batch.params[lo:hi].copy()
+    w = Workload(**{**batch.workload.__dict__, "B": hi - lo})
+    return Batch(w, target, draft, m_off, tokens, params, batch.params_dev[lo * 32:hi * 32])
+
+
 def custom_workload(**kw) -> Workload:
     """A workload with explicit fields (for small parity and edge cases)."""
     base = dict(name="custom", B=4, V=64, dtype=F32)
