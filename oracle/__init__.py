@@ -18,7 +18,7 @@ import subprocess
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "sdcp_oracle.c")
+_SRCS = [os.path.join(_HERE, "sdcp_oracle.c"), os.path.join(_HERE, "sdcp_oracle_commit.c")]
 _LIB_PATH = os.path.join(_HERE, "libsdcp_oracle.so")
 
 F32, BF16 = 0, 1
@@ -53,10 +53,11 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile the oracle (gcc, OpenMP, -O2, no -ffast-math) in place; return its path."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(f) for f in _SRCS)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
         tmp = _LIB_PATH + ".tmp%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
-                               "-o", tmp, _SRC, "-lm"])
+        subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-fopenmp", "-fPIC", "-shared",
+                               "-o", tmp] + _SRCS + ["-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -85,6 +86,26 @@ def lib():
         L.oracle_row_stats_batch.restype = ctypes.c_int
         L.oracle_set_topp_shift.argtypes = [ctypes.c_double]
         L.oracle_set_topp_shift.restype = None
+        L.oracle_verify_batch_rng.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp,
+                                              vp, vp, vp, vp, vp, vp, ctypes.c_int]
+        L.oracle_row_dist_forced.argtypes = [vp, ctypes.c_int, i64, u32, u32, u32, vp, vp,
+                                             ctypes.POINTER(RowInfo), i64]
+        L.oracle_row_dist_forced.restype = ctypes.c_int
+        L.oracle_verify_batch_rng.restype = ctypes.c_int
+        L.oracle_sha256.argtypes = [vp, ctypes.c_size_t, vp]
+        L.oracle_sha256.restype = None
+        L.oracle_hmac_sha256.argtypes = [vp, ctypes.c_size_t, vp, ctypes.c_size_t, vp]
+        L.oracle_hmac_sha256.restype = None
+        L.oracle_hmac_uniform.argtypes = [u64, vp, u32, u32, u32]
+        L.oracle_hmac_uniform.restype = ctypes.c_double
+        L.oracle_contract_digest.argtypes = [vp, ctypes.c_size_t, vp]
+        L.oracle_contract_digest.restype = None
+        L.oracle_prefix_digest.argtypes = [vp, vp, u32, vp]
+        L.oracle_prefix_digest.restype = None
+        L.oracle_digest_extend.argtypes = [vp, vp, i32, vp]
+        L.oracle_digest_extend.restype = None
+        L.oracle_commit_round.argtypes = [vp, vp, vp, i32, i32, vp, vp, u32]
+        L.oracle_commit_round.restype = i32
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = ctypes.c_int
         _lib = L
@@ -117,15 +138,18 @@ def uniform(seed: int, round_: int, position: int, purpose: int, tag: int) -> fl
 
 
 def row_dist(row: np.ndarray, temperature_milli: int = 1000, top_k: int = 0,
-             top_p_milli: int = 1000, want_dist: bool = True, want_kept: bool = False):
-    """The sampling profile of SDCP Section 4.1 on one row.  Returns (dist, kept, info, rc)."""
+             top_p_milli: int = 1000, want_dist: bool = True, want_kept: bool = False,
+             force_kept: int = -1):
+    """The sampling profile of SDCP Section 4.1 on one row.  Returns (dist, kept, info, rc).
+    force_kept >= 1 places the top-p crossing at that many tokens (parity-test hook)."""
     row = np.ascontiguousarray(row)
     V = row.shape[0]
     dist = np.zeros(V, dtype=np.float64) if want_dist else None
     kept = np.zeros(V, dtype=np.uint8) if want_kept else None
     info = RowInfo()
-    rc = lib().oracle_row_dist(_ptr(row), _dtype_code(row), V, temperature_milli, top_k,
-                               top_p_milli, _ptr(dist), _ptr(kept), ctypes.byref(info))
+    rc = lib().oracle_row_dist_forced(_ptr(row), _dtype_code(row), V, temperature_milli, top_k,
+                                      top_p_milli, _ptr(dist), _ptr(kept), ctypes.byref(info),
+                                      int(force_kept))
     return dist, kept, info, rc
 
 
@@ -147,12 +171,15 @@ def draw(p: np.ndarray, q: np.ndarray | None, u: float) -> int:
 
 def verify_batch(target: np.ndarray, draft: np.ndarray | None, m_offsets: np.ndarray,
                  draft_tokens: np.ndarray, params: np.ndarray, nthreads: int = 1,
-                 want_detail: bool = True):
+                 want_detail: bool = True, session_ids: np.ndarray | None = None,
+                 force_kept: np.ndarray | None = None):
     """Rules 1 and 2 of SDCP Section 6.4 over a ragged batch (layout of the C ABI).
 
     target: [total_drafts + B, V], draft: [total_drafts, V] or None (float32 or raw bf16
-    bits as uint16).  Returns a dict of numpy arrays (accepted, n_out, out_tokens, status,
-    detail).
+    bits as uint16).  session_ids ([B, 16] uint8) selects the draft's HMAC-SHA-256 random
+    values (Section 6.4) instead of Philox.  force_kept ([2 total + B] int32, row order of
+    the C ABI's row statistics, -1 = as defined) places top-p crossings (a parity-test
+    hook).  Returns a dict of numpy arrays (accepted, n_out, out_tokens, status, detail).
     """
     target = np.ascontiguousarray(target)
     dcode = _dtype_code(target)
@@ -171,9 +198,17 @@ def verify_batch(target: np.ndarray, draft: np.ndarray | None, m_offsets: np.nda
     toks = np.full(total + B, -1, np.int32)
     st = np.zeros(B, np.int32)
     det = np.zeros(B, DETAIL_DTYPE) if want_detail else None
-    rc = lib().oracle_verify_batch(_ptr(target), _ptr(draft), dcode, V, B, _ptr(m_offsets),
-                                   total, _ptr(draft_tokens), _ptr(params), _ptr(acc),
-                                   _ptr(nout), _ptr(toks), _ptr(st), _ptr(det), int(nthreads))
+    sid = None
+    if session_ids is not None:
+        sid = np.ascontiguousarray(session_ids, dtype=np.uint8).reshape(B, 16)
+    fk = None
+    if force_kept is not None:
+        fk = np.ascontiguousarray(force_kept, dtype=np.int32)
+        assert fk.shape == (2 * total + B,)
+    rc = lib().oracle_verify_batch_rng(_ptr(target), _ptr(draft), dcode, V, B, _ptr(m_offsets),
+                                       total, _ptr(draft_tokens), _ptr(params), _ptr(sid), _ptr(fk),
+                                       _ptr(acc), _ptr(nout), _ptr(toks), _ptr(st), _ptr(det),
+                                       int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify_batch rejected its arguments (rc=%d)" % rc)
     return {"accepted": acc, "n_out": nout, "out_tokens": toks, "status": st, "detail": det}
@@ -225,6 +260,85 @@ class topp_shift:
     def __exit__(self, *exc):
         lib().oracle_set_topp_shift(0.0)
         return False
+
+
+# ---------------------------------------------------------------------------------------
+# SHA-256, HMAC, digests, truncation and control (sdcp_oracle_commit.c)
+# ---------------------------------------------------------------------------------------
+ACT_CONTINUE, ACT_REDUCE, ACT_SWITCH, ACT_SELF_DECODE, ACT_FINISH, ACT_FAIL = 0, 1, 2, 3, 4, 5
+
+# contract terms of one session and the verifier's per-session state (layouts of
+# orc_commit_params and orc_session_state)
+COMMIT_PARAMS_DTYPE = np.dtype([("max_new", "<u4"), ("stop_offset", "<u4"), ("stop_count", "<u4"),
+                                ("m_max", "<u4"), ("low_rounds", "<u4"), ("low_ratio", "<u4"),
+                                ("self_load", "<u4"), ("fallback_len", "<u4"), ("fallback", "u1", (8,)),
+                                ("m_restore", "<u4"), ("pad", "<u4")])
+STATE_DTYPE = np.dtype([("digest", "u1", (32,)), ("committed", "<u4"), ("c", "<u4"), ("g", "<u4"),
+                        ("j", "<u4"), ("m_cap", "<u4"), ("pad", "<u4", (3,))])
+
+
+def _bytes_in(b: bytes):
+    a = np.frombuffer(bytes(b), dtype=np.uint8).copy()
+    return a, (a.ctypes.data_as(ctypes.c_void_p) if a.size else None)
+
+
+def sha256(msg: bytes) -> bytes:
+    a, p = _bytes_in(msg)
+    out = np.zeros(32, np.uint8)
+    lib().oracle_sha256(p, len(msg), _ptr(out))
+    return out.tobytes()
+
+
+def hmac_sha256(key: bytes, msg: bytes) -> bytes:
+    k, kp = _bytes_in(key)
+    m, mp = _bytes_in(msg)
+    out = np.zeros(32, np.uint8)
+    lib().oracle_hmac_sha256(kp, len(key), mp, len(msg), _ptr(out))
+    return out.tobytes()
+
+
+def hmac_uniform(seed: int, session: bytes, round_: int, i: int, purpose: int) -> float:
+    s, sp = _bytes_in(session)
+    assert len(session) == 16
+    return lib().oracle_hmac_uniform(seed, sp, round_, i, purpose)
+
+
+def contract_digest(cbor: bytes) -> bytes:
+    c, cp = _bytes_in(cbor)
+    out = np.zeros(32, np.uint8)
+    lib().oracle_contract_digest(cp, len(cbor), _ptr(out))
+    return out.tobytes()
+
+
+def prefix_digest(contract_dig: bytes, prompt) -> bytes:
+    c, cp = _bytes_in(contract_dig)
+    t = np.ascontiguousarray(np.asarray(prompt, dtype=np.uint32))
+    out = np.zeros(32, np.uint8)
+    lib().oracle_prefix_digest(cp, _ptr(t) if t.size else None, len(t), _ptr(out))
+    return out.tobytes()
+
+
+def digest_extend(d: bytes, tokens) -> bytes:
+    c, cp = _bytes_in(d)
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    out = np.zeros(32, np.uint8)
+    lib().oracle_digest_extend(cp, _ptr(t) if t.size else None, len(t), _ptr(out))
+    return out.tobytes()
+
+
+def commit_round(cparams: np.ndarray, stop_tokens, state: np.ndarray, a: int, M: int,
+                 emitted, load: int = 0):
+    """One session's round after acceptance (SDCP Sections 6.3 and 6.5): truncation, commit,
+    control.  state ([1] STATE_DTYPE) is updated in place; returns (action, emitted)."""
+    cp = np.ascontiguousarray(cparams, dtype=COMMIT_PARAMS_DTYPE).reshape(1)
+    st = np.asarray([0] if stop_tokens is None or len(stop_tokens) == 0 else stop_tokens, dtype=np.uint32)
+    st = np.ascontiguousarray(st)
+    toks = np.ascontiguousarray(np.asarray(emitted, dtype=np.int32)).copy()
+    n = np.asarray([len(toks)], np.int32)
+    assert state.dtype == STATE_DTYPE and state.flags["C_CONTIGUOUS"]
+    act = lib().oracle_commit_round(_ptr(cp), _ptr(st), _ptr(state), int(a), int(M), _ptr(n),
+                                    _ptr(toks) if toks.size else None, int(load))
+    return int(act), [int(v) for v in toks[:int(n[0])]]
 
 
 def max_threads() -> int:

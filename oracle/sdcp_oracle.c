@@ -125,6 +125,20 @@ double oracle_uniform(uint64_t seed, uint32_t round, uint32_t position, uint32_t
   return (double)bits53 * (1.0 / 9007199254740992.0); /* 2^53 */
 }
 
+/* The draft's own derivation (Section 6.4, last paragraph): HMAC-SHA-256 keyed with the
+   seed over the session identifier, round, 1-based position and purpose (in
+   sdcp_oracle_commit.c). */
+double oracle_hmac_uniform(uint64_t seed, const uint8_t session[16], uint32_t round, uint32_t i,
+                           uint32_t purpose);
+
+/* The verifier's random value for 0-based position `pos` and `purpose`: Philox when sid is
+   NULL, else the HMAC derivation with the session's 16-octet identifier sid and the
+   1-based position pos + 1. */
+static double verifier_uniform(const orc_params* p, const uint8_t* sid, uint32_t pos, uint32_t purpose) {
+  if (sid) return oracle_hmac_uniform(p->seed, sid, p->round, pos + 1u, purpose);
+  return oracle_uniform(p->seed, p->round, pos, purpose, p->session_tag);
+}
+
 /* ---------------------------------------------------------------------------------- */
 /* Logit access: bf16 is the upper half of a binary32, so both widen to double exactly. */
 /* ---------------------------------------------------------------------------------- */
@@ -159,11 +173,15 @@ static int cmp_desc(const void* a, const void* b) {
 /*
  * The sampling profile of Section 4.1 applied to one row of logits.
  * dist (optional, [V]): the fp64 distribution; kept (optional, [V]): 1 for kept ids.
+ * force_k2 >= 1 (a test hook; -1 otherwise) places the top-p crossing at that many tokens
+ * instead of where the cumulative mass first reaches P: the parity tests use it, for a row
+ * whose crossing lies within rounding of P, to form the distribution of the crossing the
+ * GPU chose (info still records the crossing of the definition).
  * Returns 0, or 1 when the row holds NaN, +inf or no finite logit.
  */
-int oracle_row_dist(const void* row, int dtype, int64_t V, uint32_t temperature_milli,
-                    uint32_t top_k, uint32_t top_p_milli, double* dist, uint8_t* kept,
-                    orc_row_info* info) {
+static int row_dist_impl(const void* row, int dtype, int64_t V, uint32_t temperature_milli,
+                         uint32_t top_k, uint32_t top_p_milli, double* dist, uint8_t* kept,
+                         orc_row_info* info, int64_t force_k2) {
   orc_row_info local;
   if (!info) info = &local;
   memset(info, 0, sizeof *info);
@@ -231,6 +249,7 @@ int oracle_row_dist(const void* row, int dtype, int64_t V, uint32_t temperature_
     info->topp_cum_before = before;
     info->topp_cum_at = cum;
     info->topp_target = target;
+    if (force_k2 >= 1) k2 = force_k2 < k1 ? force_k2 : k1;
   }
 
   /* Renormalise over the final kept set (same order of summation). */
@@ -246,6 +265,19 @@ int oracle_row_dist(const void* row, int dtype, int64_t V, uint32_t temperature_
   free(pi);
   free(ord);
   return 0;
+}
+
+int oracle_row_dist(const void* row, int dtype, int64_t V, uint32_t temperature_milli,
+                    uint32_t top_k, uint32_t top_p_milli, double* dist, uint8_t* kept,
+                    orc_row_info* info) {
+  return row_dist_impl(row, dtype, V, temperature_milli, top_k, top_p_milli, dist, kept, info, -1);
+}
+
+int oracle_row_dist_forced(const void* row, int dtype, int64_t V, uint32_t temperature_milli,
+                           uint32_t top_k, uint32_t top_p_milli, double* dist, uint8_t* kept,
+                           orc_row_info* info, int64_t force_k2) {
+  return row_dist_impl(row, dtype, V, temperature_milli, top_k, top_p_milli, dist, kept, info,
+                       force_k2);
 }
 
 /*
@@ -370,9 +402,9 @@ static double topp_margin_of(const orc_row_info* in) {
 /* One session, Sections 6.3 and 6.4. */
 static void verify_session(const void* T, const void* D, int dtype, int64_t V,
                            const int32_t* m_offsets, int64_t total_drafts, int32_t b,
-                           const int32_t* x, const orc_params* prm, int32_t* accepted,
-                           int32_t* n_out, int32_t* out_tokens, int32_t* status,
-                           orc_detail* det) {
+                           const int32_t* x, const orc_params* prm, const uint8_t* sid,
+                           const int32_t* force, int64_t R_T, int32_t* accepted, int32_t* n_out,
+                           int32_t* out_tokens, int32_t* status, orc_detail* det) {
   size_t esz = (dtype == ORC_F32) ? 4 : 2;
   orc_detail dl;
   if (!det) det = &dl;
@@ -398,6 +430,10 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
   uint32_t tm = prm->temperature_milli;
 #define TROW(i) ((const char*)T + (size_t)(off0 + b + (i)) * (size_t)V * esz)
 #define DROW(i) ((const char*)D + (size_t)(off0 + (i)) * (size_t)V * esz)
+  /* forced top-p crossings (test hook), indexed like the C ABI's row statistics:
+     target rows first, then the draft rows from R_T = total_drafts + B */
+#define FT(i) (force ? (int64_t)force[off0 + b + (i)] : -1)
+#define FD(i) (force ? (int64_t)force[R_T + off0 + (i)] : -1)
 
   /* Every scored row is formed before any draw: p for the M+1 target rows, q for the
      M draft rows (Rule 2).  Rule 1 needs only the argmax of the raw scores. */
@@ -409,8 +445,8 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
     for (int64_t i = 0; i <= M && st == ORC_OK; ++i) {
       if (rule2) {
         pk[i] = (uint8_t*)malloc((size_t)V);
-        if (oracle_row_dist(TROW(i), dtype, V, tm, prm->top_k, prm->top_p_milli, NULL,
-                            pk[i], &pin[i]))
+        if (row_dist_impl(TROW(i), dtype, V, tm, prm->top_k, prm->top_p_milli, NULL,
+                          pk[i], &pin[i], FT(i)))
           st = ORC_BAD_PARAMS;
       } else if (oracle_row_dist(TROW(i), dtype, V, 0, 0, 1000, NULL, NULL, &pin[i])) {
         st = ORC_BAD_PARAMS;
@@ -423,8 +459,8 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
       qk = (uint8_t**)calloc((size_t)M, sizeof(uint8_t*));
       for (int64_t i = 0; i < M && st == ORC_OK; ++i) {
         qk[i] = (uint8_t*)malloc((size_t)V);
-        if (oracle_row_dist(DROW(i), dtype, V, tm, prm->top_k, prm->top_p_milli, NULL,
-                            qk[i], &qin[i]))
+        if (row_dist_impl(DROW(i), dtype, V, tm, prm->top_k, prm->top_p_milli, NULL,
+                          qk[i], &qin[i], FD(i)))
           st = ORC_BAD_PARAMS;
         double mg = topp_margin_of(&qin[i]);
         if (mg < det->topp_margin) det->topp_margin = mg;
@@ -464,7 +500,7 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
       }
       double ratio = (lp == -INFINITY) ? 0.0 : exp(lp - lq);
       if (ratio > 1.0) ratio = 1.0;
-      double u = oracle_uniform(prm->seed, prm->round, (uint32_t)a, 0, prm->session_tag);
+      double u = verifier_uniform(prm, sid, (uint32_t)a, 0);
       det->log_p[a] = lp; det->log_q[a] = lq; det->u0[a] = u; det->ratio[a] = ratio;
       if (!(u < ratio)) break; /* first rejection */
     }
@@ -472,9 +508,9 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
     double* pa = (double*)malloc(sizeof(double) * (size_t)V);
     double* qa = (a < M) ? (double*)malloc(sizeof(double) * (size_t)V) : NULL;
     double* C = (double*)malloc(sizeof(double) * (size_t)V);
-    oracle_row_dist(TROW(a), dtype, V, tm, prm->top_k, prm->top_p_milli, pa, NULL, NULL);
-    if (qa) oracle_row_dist(DROW(a), dtype, V, tm, prm->top_k, prm->top_p_milli, qa, NULL, NULL);
-    double u1 = oracle_uniform(prm->seed, prm->round, (uint32_t)a, 1, prm->session_tag);
+    row_dist_impl(TROW(a), dtype, V, tm, prm->top_k, prm->top_p_milli, pa, NULL, NULL, FT(a));
+    if (qa) row_dist_impl(DROW(a), dtype, V, tm, prm->top_k, prm->top_p_milli, qa, NULL, NULL, FD(a));
+    double u1 = verifier_uniform(prm, sid, (uint32_t)a, 1);
     det->u1 = u1;
     if (qa) {
       extra = draw_from(pa, qa, V, u1, C, &det->W, &det->c_lo, &det->c_hi);
@@ -491,6 +527,8 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
   }
 #undef TROW
 #undef DROW
+#undef FT
+#undef FD
 
   /* Outputs (Section 5.2): a accepted tokens, then the additional token. */
   status[b] = st;
@@ -523,11 +561,15 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
  * proposals of many sessions), so nthreads > 1 runs them on OpenMP threads.
  * detail (optional, [B]) records every decision of every session.
  */
-int oracle_verify_batch(const void* T, const void* D, int dtype, int64_t V, int32_t B,
-                        const int32_t* m_offsets, int64_t total_drafts,
-                        const int32_t* draft_tokens, const orc_params* params,
-                        int32_t* accepted, int32_t* n_out, int32_t* out_tokens,
-                        int32_t* status, orc_detail* detail, int nthreads) {
+/* session_ids (optional, [B][16]) selects the HMAC derivation of the random values;
+   force_kept (optional, [2 total + B], row order of the C ABI's row statistics) is the
+   parity tests' hook that places top-p crossings (-1: where the definition puts them). */
+int oracle_verify_batch_rng(const void* T, const void* D, int dtype, int64_t V, int32_t B,
+                            const int32_t* m_offsets, int64_t total_drafts,
+                            const int32_t* draft_tokens, const orc_params* params,
+                            const uint8_t* session_ids, const int32_t* force_kept,
+                            int32_t* accepted, int32_t* n_out, int32_t* out_tokens,
+                            int32_t* status, orc_detail* detail, int nthreads) {
   if (B < 0 || V < 1 || (dtype != ORC_F32 && dtype != ORC_BF16)) return 1;
   if (!T || !m_offsets || !draft_tokens || !params) return 1;
 #ifdef _OPENMP
@@ -536,8 +578,21 @@ int oracle_verify_batch(const void* T, const void* D, int dtype, int64_t V, int3
 #endif
   for (int32_t b = 0; b < B; ++b)
     verify_session(T, D, dtype, V, m_offsets, total_drafts, b, draft_tokens, &params[b],
-                   accepted, n_out, out_tokens, status, detail ? &detail[b] : NULL);
+                   session_ids ? session_ids + 16 * (size_t)b : NULL, force_kept,
+                   total_drafts + B, accepted, n_out, out_tokens, status,
+                   detail ? &detail[b] : NULL);
   return 0;
+}
+
+/* The whole batch with Philox random values. */
+int oracle_verify_batch(const void* T, const void* D, int dtype, int64_t V, int32_t B,
+                        const int32_t* m_offsets, int64_t total_drafts,
+                        const int32_t* draft_tokens, const orc_params* params,
+                        int32_t* accepted, int32_t* n_out, int32_t* out_tokens,
+                        int32_t* status, orc_detail* detail, int nthreads) {
+  return oracle_verify_batch_rng(T, D, dtype, V, B, m_offsets, total_drafts, draft_tokens,
+                                 params, NULL, NULL, accepted, n_out, out_tokens, status, detail,
+                                 nthreads);
 }
 
 int oracle_max_threads(void) {

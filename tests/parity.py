@@ -8,12 +8,13 @@ arithmetic, and then the GPU's outcome must be the one on the other side of that
   * draw: u * W within 1e-5 * W of the edge shared by the oracle's token and the GPU's
     token, which must be neighbours among the tokens of positive weight (ids ascending);
   * top-p crossing (SDCP Section 4.1): where a row's cumulative mass lies within 1e-5 of
-    P, the session must match the oracle exactly under one of the two readings of the
-    crossing (the oracle's top-p target times 1 - 1e-5 or 1 + 1e-5).
+    P, any crossing between the oracle's crossings for P (1 - 1e-5) and P (1 + 1e-5) is a
+    faithful reading; the GPU's crossing must lie in that band, and the session must then
+    match the oracle run with the GPU's crossing (under the rules above).
 Such cases are counted and returned, never silently accepted.
 Row statistics: lmax, argmax and the kept count exactly, log S and log p(x) within 1e-5
-(fp32 logits) or 2e-3 (bf16 logits); a row at a top-p boundary must match one of the two
-readings of its crossing.
+(fp32 logits) or 2e-3 (bf16 logits); a row at a top-p boundary must keep a count inside
+the band, and its log S and log p(x) must match the oracle's at that count.
 """
 from __future__ import annotations
 
@@ -68,12 +69,17 @@ def session_outputs(got, off, b):
             "n_out": got["n_out"][b:b + 1], "out_tokens": got["out_tokens"][o0 + b:o1 + b + 1]}
 
 
-def _draw_cdf(T, D, off, b, a, prm, mode):
-    """Oracle cumulative weights (ids ascending) of the draw of session b at position a."""
+def _draw_cdf(T, D, off, b, a, prm, mode, force=None):
+    """Oracle cumulative weights (ids ascending) of the draw of session b at position a
+    (force: top-p crossings per row, in the row order of the C ABI's row statistics)."""
     s = int(off[b]) + b + a
+    d = int(off[b]) + a
+    R_T = int(off[-1]) + (off.shape[0] - 1)
     tm, k, p = int(prm["temperature_milli"]), int(prm["top_k"]), int(prm["top_p_milli"])
-    pa = oracle.row_dist(T[s], tm, k, p)[0]
-    qa = oracle.row_dist(D[int(off[b]) + a], tm, k, p)[0] if mode == oracle.EXTRA_RESIDUAL else None
+    fp = -1 if force is None else int(force[s])
+    fq = -1 if force is None else int(force[R_T + d])
+    pa = oracle.row_dist(T[s], tm, k, p, force_kept=fp)[0]
+    qa = oracle.row_dist(D[d], tm, k, p, force_kept=fq)[0] if mode == oracle.EXTRA_RESIDUAL else None
     return oracle.draw_cdf(pa, qa)
 
 
@@ -99,8 +105,50 @@ def _check_draw_boundary(C, W, u1, tg, to, b):
             b, tg, to, target, abs(target - edge), W))
 
 
-def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok):
-    """One session; adds to counts; raises AssertionError on a real disagreement."""
+def topp_band(logits, tm, k, p):
+    """Kept counts of the oracle's top-p crossing for P (1 - 1e-5) and P (1 + 1e-5)."""
+    with oracle.topp_shift(-BOUNDARY):
+        lo = oracle.row_dist(logits, tm, k, p, want_dist=False)[2].kept
+    with oracle.topp_shift(BOUNDARY):
+        hi = oracle.row_dist(logits, tm, k, p, want_dist=False)[2].kept
+    return int(lo), int(hi)
+
+
+def _row_margin(info):
+    if info.topp_target < 0:
+        return np.inf
+    return min(abs(info.topp_cum_at - info.topp_target),
+               abs(info.topp_cum_before - info.topp_target)) / info.topp_target
+
+
+def _forced_session(T, D, off, x, params, b, gs):
+    """The oracle on session b alone with the GPU's top-p crossings at the session's
+    boundary rows (each checked to lie in its band)."""
+    B = params.shape[0]
+    total = int(off[-1])
+    R_T = total + B
+    args = session_arrays(T, D, off, x, params, b)
+    Ts, Ds = args[0], args[1]
+    M = Ts.shape[0] - 1
+    prm = params[b]
+    tm, k, p = int(prm["temperature_milli"]), int(prm["top_k"]), int(prm["top_p_milli"])
+    force = np.full(2 * M + 1, -1, np.int32)
+    o0 = int(off[b])
+    rows = [(i, Ts[i], o0 + b + i) for i in range(M + 1)] + [(M + 1 + i, Ds[i], R_T + o0 + i) for i in range(M)]
+    for j, logits, r in rows:
+        info = oracle.row_dist(logits, tm, k, p, want_dist=False)[2]
+        if info.invalid or _row_margin(info) > BOUNDARY:
+            continue
+        n = int(gs[r]["kept"])
+        lo, hi = topp_band(logits, tm, k, p)
+        assert lo <= n <= hi, ("session %d row %d: GPU crossing %d outside the band [%d, %d]" % (b, r, n, lo, hi))
+        force[j] = n
+    return args, force, oracle.verify_batch(*args, force_kept=force)
+
+
+def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None, force=None):
+    """One session; adds to counts; raises AssertionError on a real disagreement.  force:
+    the top-p crossings ref was computed with (None: as defined)."""
     det = ref["detail"]
     o0, o1 = int(off[b]), int(off[b + 1])
     slot = slice(o0 + b, o1 + b + 1) if 0 <= o0 <= o1 else slice(0, 0)
@@ -114,23 +162,30 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok):
     assert rule == 2, "greedy session %d differs: gpu a=%d tokens=%s, oracle a=%d tokens=%s" % (
         b, got["accepted"][b], got["out_tokens"][slot], ref["accepted"][b], ref["out_tokens"][slot])
     if topp_ok and det["topp_margin"][b] <= BOUNDARY:
-        # a top-p crossing within rounding of P: the session must match the oracle under one
-        # of the two readings of that crossing
-        args = session_arrays(T, D, off, x, params, b)
+        # a top-p crossing within rounding of P: the session must match the oracle run with
+        # the GPU's crossings (each inside its band), or, without the GPU's row statistics,
+        # the oracle under one of the band's two ends
         mine = session_outputs(got, off, b)
-        errs = []
-        for shift in (-BOUNDARY, BOUNDARY):
-            with oracle.topp_shift(shift):
-                r2 = oracle.verify_batch(*args)
+        if gs is not None:
+            args, force2, r2 = _forced_session(T, D, off, x, params, b, gs)
             c2 = {"exact": 0, "accept_boundary": 0, "draw_boundary": 0, "topp_boundary": 0}
-            try:
-                _compare_session(mine, r2, *args, 0, c2, topp_ok=False)
-            except AssertionError as e:
-                errs.append(str(e))
-                continue
+            _compare_session(mine, r2, *args, 0, c2, topp_ok=False, force=force2)
             counts["topp_boundary"] += 1
             return
-        raise AssertionError("session %d matches neither reading of its top-p crossing: %s" % (b, errs))
+        args = session_arrays(T, D, off, x, params, b)
+        errs = []
+        for shift in (-BOUNDARY, BOUNDARY):
+            c2 = {"exact": 0, "accept_boundary": 0, "draw_boundary": 0, "topp_boundary": 0}
+            with oracle.topp_shift(shift):
+                r2 = oracle.verify_batch(*args)
+                try:
+                    _compare_session(mine, r2, *args, 0, c2, topp_ok=False)
+                except AssertionError as e:
+                    errs.append(str(e))
+                    continue
+            counts["topp_boundary"] += 1
+            return
+        raise AssertionError("session %d matches neither end of its top-p band: %s" % (b, errs))
     ag, ao = int(got["accepted"][b]), int(ref["accepted"][b])
     if ag != ao:
         i = min(ag, ao)
@@ -148,7 +203,7 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok):
     mode = int(det["extra_mode"][b])
     assert mode in (oracle.EXTRA_RESIDUAL, oracle.EXTRA_BONUS, oracle.EXTRA_RESIDUAL_AS_P), mode
     m2 = oracle.EXTRA_RESIDUAL if mode == oracle.EXTRA_RESIDUAL else oracle.EXTRA_BONUS
-    C, W = _draw_cdf(T, D, off, b, a, params[b], m2)
+    C, W = _draw_cdf(T, D, off, b, a, params[b], m2, force)
     _check_draw_boundary(C, W, float(det["u1"][b]), int(gt[a]), int(rt[a]), b)
     counts["draw_boundary"] += 1
     # only the drawn slot may differ
@@ -156,14 +211,16 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok):
                           ref["out_tokens"][o0 + b + a + 1:o1 + b + 1])
 
 
-def compare_verdicts(got, ref, T, D, off, x, params):
-    """Returns a dict of counts; raises AssertionError on a real disagreement."""
+def compare_verdicts(got, ref, T, D, off, x, params, gs=None):
+    """Returns a dict of counts; raises AssertionError on a real disagreement.  gs: the
+    GPU's row statistics of the same batch (sdcp_row_stats), used where a top-p crossing
+    lies within rounding of P."""
     B = params.shape[0]
     counts = {"sessions": B, "exact": 0, "accept_boundary": 0, "draw_boundary": 0,
               "topp_boundary": 0}
     assert np.array_equal(got["status"], ref["status"]), (got["status"], ref["status"])
     for b in range(B):
-        _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok=True)
+        _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok=True, gs=gs)
     return counts
 
 
@@ -237,7 +294,8 @@ def compare_row_stats(gs, T, D, off, x, params, dtype_code, rows=None):
     assert bad.size == 0, ("log S differs", sel[bad[:5]], gls[bad[:5]], o["log_s"][bad[:5]])
     glp = g["lp_x"].astype(np.float64)
     fin = nb & np.isfinite(lp)
-    bad = np.nonzero(fin & ~(np.abs(glp - lp) <= tol * np.maximum(1.0, np.abs(lp))))[0]
+    with np.errstate(invalid="ignore"):
+        bad = np.nonzero(fin & ~(np.abs(glp - lp) <= tol * np.maximum(1.0, np.abs(lp))))[0]
     assert bad.size == 0, ("log p(x) differs", sel[bad[:5]], glp[bad[:5]], lp[bad[:5]])
     ninf = nb & np.isneginf(lp)
     bad = np.nonzero(ninf & ~np.isneginf(glp))[0]
@@ -245,25 +303,27 @@ def compare_row_stats(gs, T, D, off, x, params, dtype_code, rows=None):
     nan = nb & np.isnan(lp)
     bad = np.nonzero(nan & ~np.isnan(glp))[0]
     assert bad.size == 0, ("log p(x) should be NaN (no draft token)", sel[bad[:5]], glp[bad[:5]])
-    # rows at a top-p boundary: the GPU's kept set must be one of the two readings
+    # rows at a top-p boundary: the GPU's crossing must lie in the band, and the row's
+    # statistics must match the oracle's with that crossing
     for i in np.nonzero(topp_b)[0]:
         r = int(sel[i])
         b, xi = _row_session(off, B, total, r)
         prm = params[b]
         tm, k, p = int(prm["temperature_milli"]), int(prm["top_k"]), int(prm["top_p_milli"])
         logits = _row_logits(T, D, R_T, r)
-        matched = False
-        for shift in (-BOUNDARY, BOUNDARY):
-            with oracle.topp_shift(shift):
-                dist, kept, inf2, rc = oracle.row_dist(logits, tm, k, p, want_kept=True)
-            if int(g["kept"][i]) != int(inf2.kept):
-                continue
-            if not abs(gls[i] - inf2.log_s) <= tol * max(1.0, abs(inf2.log_s)):
-                continue
-            matched = True
-            break
-        assert matched, ("row %d at a top-p boundary matches neither reading" % r, int(g["kept"][i]),
-                         int(o["kept"][i]))
+        n = int(g["kept"][i])
+        lo, hi = topp_band(logits, tm, k, p)
+        assert lo <= n <= hi, ("row %d: GPU crossing %d outside the band [%d, %d]" % (r, n, lo, hi))
+        dist, kept, inf2, rc = oracle.row_dist(logits, tm, k, p, want_kept=True, force_kept=n)
+        assert int(inf2.kept) == n
+        assert abs(gls[i] - inf2.log_s) <= tol * max(1.0, abs(inf2.log_s)), (r, gls[i], inf2.log_s)
+        if xi is not None and 0 <= int(x[xi]) < len(dist):
+            xv = int(x[xi])
+            if kept[xv] and dist[xv] > 0:
+                lpv = np.log(dist[xv])
+                assert abs(glp[i] - lpv) <= tol * max(1.0, abs(lpv)), (r, glp[i], lpv)
+            else:
+                assert np.isneginf(glp[i]), (r, glp[i])
     return {"rows": int(sel.size), "topp_boundary": int(topp_b.sum()),
             "fallback": int(((flags & ROW_FALLBACK) != 0).sum())}
 

@@ -34,10 +34,10 @@ def _parity(batch, rows=True, with_draft=True, name=None):
     T, D, off, x = parity.host_arrays(batch)
     ref = oracle.verify_batch(T, D if with_draft else None, off, x, batch.params,
                               nthreads=parity.ORACLE_THREADS)
-    counts = parity.compare_verdicts(got, ref, T, D, off, x, batch.params)
+    gs = parity.gpu_row_stats(batch) if rows else None
+    counts = parity.compare_verdicts(got, ref, T, D, off, x, batch.params, gs=gs)
     parity.check_invariants(got, off, x, batch.params, batch.V)
     if rows:
-        gs = parity.gpu_row_stats(batch)
         counts["rows"] = parity.compare_row_stats(gs, T, D, off, x, batch.params, batch.dtype_code)
     if name is not None:
         parity.report(name, counts)
