@@ -240,6 +240,110 @@ int sdcp_verify_batch_noalloc(const void* target_logits, const void* draft_logit
                               int32_t* n_out, int32_t* out_tokens, int32_t* status,
                               void* stream);
 
+/* ---- random values of the acceptance step --------------------------------------- */
+#define SDCP_RNG_PHILOX4X32_10 0  /* counter-based Philox (the default, described above) */
+#define SDCP_RNG_HMAC_SHA256   1  /* the draft's own derivation (Section 6.4, last
+                                     paragraph): HMAC-SHA-256 keyed with the seed as eight
+                                     octets in network order, over "SDCP-VERIFY-1" || 0x00
+                                     || session (16 octets) || uint32(round) || uint32(i) ||
+                                     uint8(purpose), the first 53 bits / 2^53; i is the
+                                     1-based position of the pages (the acceptance test of
+                                     0-based position k uses i = k + 1, the additional token
+                                     after a accepted tokens i = a + 1) */
+
+/* Options of sdcp_verify_batch_ex (host struct). */
+typedef struct sdcp_verify_options {
+  uint32_t struct_size;         /* sizeof(sdcp_verify_options) */
+  uint32_t rng_id;              /* SDCP_RNG_* */
+  const uint8_t* session_ids;   /* device, [B][16]: each session's 16-octet identifier
+                                   (Section 5.2 session-id); needed by SDCP_RNG_HMAC_SHA256,
+                                   ignored by Philox (which uses params[b].session_tag) */
+} sdcp_verify_options;
+
+/*
+ * sdcp_verify_batch with options: the same arguments, layout and results, with the random
+ * values chosen by opts->rng_id.  opts = NULL is sdcp_verify_batch.  Returns SDCP_E_INVALID
+ * for an unknown rng_id, a struct_size below sizeof(sdcp_verify_options), or the HMAC
+ * generator without session_ids.
+ */
+int sdcp_verify_batch_ex(const void* target_logits, const void* draft_logits, int dtype,
+                         int64_t V, int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                         const int32_t* draft_tokens, const sdcp_session_params* params,
+                         int32_t* accepted, int32_t* n_out, int32_t* out_tokens,
+                         int32_t* status, void* workspace, size_t workspace_bytes,
+                         const sdcp_verify_options* opts, void* stream);
+
+/* ---- the commit step after acceptance (Sections 4.2, 6.3, 6.5) ------------------- */
+/* actions of a verdict (Section 4.1 "action"; Section 6.5.2) */
+#define SDCP_ACTION_NONE        (-1) /* the session's status was not SDCP_S_OK: nothing
+                                        committed, its state unchanged */
+#define SDCP_ACTION_CONTINUE    0
+#define SDCP_ACTION_REDUCE      1
+#define SDCP_ACTION_SWITCH      2
+#define SDCP_ACTION_SELF_DECODE 3
+#define SDCP_ACTION_FINISH      4
+#define SDCP_ACTION_FAIL        5
+#define SDCP_NO_SELF_LOAD  0xFFFFFFFFu  /* the contract has no self_load member */
+
+/* The contract terms of one session the commit step uses (Section 4.1), 48 bytes, device. */
+typedef struct sdcp_commit_params {
+  uint32_t max_new;       /* maximum output tokens of the session */
+  uint32_t stop_offset;   /* its stop tokens are stop_tokens[stop_offset .. +stop_count) */
+  uint32_t stop_count;
+  uint32_t m_max;         /* upper bound on M (<= SDCP_MAX_M); caps m_cap */
+  uint32_t low_rounds;    /* R >= 1, the escalation period */
+  uint32_t low_ratio;     /* percent 0..100; 0 = absent (a round is low iff a = 0) */
+  uint32_t self_load;     /* percent 0..100, or SDCP_NO_SELF_LOAD */
+  uint32_t fallback_len;  /* 1..8 entries of fallback[] */
+  uint8_t fallback[8];    /* the ladder: SDCP_ACTION_REDUCE, _SWITCH, _SELF_DECODE, _FAIL */
+  uint32_t m_restore;     /* after a round that is not low, m_cap grows by this, up to m_max
+                             (Section 6.5.1: "restore gradually"; 0 = never) */
+  uint32_t reserved;
+} sdcp_commit_params;
+
+/* The verifier's per-session state between rounds, 64 bytes, device; read and updated. */
+typedef struct sdcp_session_state {
+  uint8_t digest[32];     /* d[n], the committed-prefix digest (Section 4.2) */
+  uint32_t committed;     /* n, the committed length */
+  uint32_t c, g, j;       /* consecutive low rounds, consecutive rounds not low, position in
+                             the fallback list (Section 6.5.2) */
+  uint32_t m_cap;         /* the largest M of the next round (Section 6.5.1); set it to
+                             m_init before the first round */
+  uint32_t reserved[3];
+} sdcp_session_state;
+
+/*
+ * The commit step of one batch, after sdcp_verify_batch on the same stream (Section 6.3,
+ * steps "Acceptance" (its truncation), "Commit" and "Control"; Sections 4.2 and 6.5).  For
+ * each session b whose status is SDCP_S_OK:
+ *   - truncation: the emitted tokens out_tokens[m_offsets[b] + b ..][0 .. n_out[b]) are
+ *     cut after the first stop token of the session (the stop token itself is emitted)
+ *     and to at most max_new - committed tokens; n_out[b] is lowered in place and the
+ *     dropped slots set to -1;
+ *   - commit: state.digest becomes d[n + m] by d[k] = SHA-256(d[k-1] || uint32(o[k])) over
+ *     the m tokens kept, and state.committed grows by m;
+ *   - control: the round is low if 100 a < low_ratio M (or, with low_ratio 0, if a = 0),
+ *     with a = accepted[b] and M = m_offsets[b+1] - m_offsets[b]; the counters c, g, j and
+ *     m_cap follow Section 6.5.2 (the ladder entry j applies when c reaches R, skipping
+ *     self_decode unless self_load is present and load_percent <= self_load; "fail" when no
+ *     entry remains; reduce halves m_cap, at least 1); a round that emitted a stop token or
+ *     reached max_new gets SDCP_ACTION_FINISH instead (its counters are still updated, no
+ *     ladder entry is applied).
+ *   action[b] receives the SDCP_ACTION_* of the round (SDCP_ACTION_NONE for a session whose
+ *   status is not SDCP_S_OK; its state, n_out and tokens are left as they are).
+ * All pointers are device memory: m_offsets, accepted, status [B] / [B+1] as written by
+ * sdcp_verify_batch; n_out, out_tokens in/out; cparams [B]; stop_tokens [sum of
+ * stop_count] (may be NULL when every stop_count is 0); state [B] in/out; action [B] out.
+ * Asynchronous on `stream`; allocates nothing.  Returns SDCP_OK, SDCP_E_INVALID (null
+ * pointer, B < 0) or SDCP_E_LAUNCH.  Contract terms out of range (low_rounds 0,
+ * fallback_len > 8) are read as the nearest valid value (1, 8).
+ */
+int sdcp_commit_batch(int32_t B, const int32_t* m_offsets, const int32_t* accepted,
+                      int32_t* n_out, int32_t* out_tokens, const int32_t* status,
+                      const sdcp_commit_params* cparams, const uint32_t* stop_tokens,
+                      sdcp_session_state* state, uint32_t load_percent, int32_t* action,
+                      void* stream);
+
 /*
  * Host-side split of one ragged batch into n_parts contiguous blocks of sessions for
  * n_parts GPUs (one process per GPU).  Sessions are independent (Section 6.3 "Scoring":

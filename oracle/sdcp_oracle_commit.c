@@ -259,20 +259,24 @@ int32_t oracle_commit_round(const orc_commit_params* cp, const uint32_t* stop_to
   oracle_digest_extend(st->digest, out_tokens, n, st->digest);
   st->committed += (uint32_t)n;
 
-  /* Section 6.5.2: is the round low? */
-  int low = (cp->low_ratio != 0) ? (100u * (uint32_t)a < cp->low_ratio * (uint32_t)M) : (a == 0);
+  /* Section 6.5.2: is the round low?  (The contract requires low_rounds >= 1 and at most
+     eight ladder entries here; other values are read as the nearest valid one.) */
+  const uint32_t R = cp->low_rounds < 1 ? 1 : cp->low_rounds;
+  const uint32_t nfb = cp->fallback_len > 8 ? 8 : cp->fallback_len;
+  int low = (cp->low_ratio != 0) ? ((uint64_t)100 * (uint32_t)a < (uint64_t)cp->low_ratio * (uint32_t)M)
+                                 : (a == 0);
   if (low) { st->c += 1; st->g = 0; }
   else {
     st->c = 0; st->g += 1;
-    if (st->g >= cp->low_rounds) st->j = 0;
+    if (st->g >= R) st->j = 0;
     uint32_t mc = st->m_cap + cp->m_restore;
     st->m_cap = mc > cp->m_max ? cp->m_max : mc;
   }
   if (finished) return ACT_FINISH;
   int32_t action = ACT_CONTINUE;
-  if (st->c >= cp->low_rounds) {
+  if (st->c >= R) {
     action = ACT_FAIL; /* unless an entry remains */
-    while (st->j < cp->fallback_len) {
+    while (st->j < nfb) {
       uint8_t e = cp->fallback[st->j];
       st->j += 1;
       if (e == ACT_SELF_DECODE && !(cp->self_load <= 100 && load <= cp->self_load)) continue;

@@ -56,7 +56,8 @@ SessIO make_io(const void* target, const void* draft, int64_t V, int32_t B, cons
   char* w = static_cast<char*>(ws);
   return SessIO{target, draft, V, B, m_offsets, total, tokens, params,
                 reinterpret_cast<const RowStat*>(w + kWsHeader),
-                accepted, n_out, out_tokens, status, reinterpret_cast<const uint32_t*>(w)};
+                accepted, n_out, out_tokens, status, reinterpret_cast<const uint32_t*>(w),
+                SDCP_RNG_PHILOX4X32_10, nullptr};
 }
 
 // Clears the header, then launches the row kernel.
@@ -109,7 +110,8 @@ static int verify_sessions(const void* target_logits, const void* draft_logits, 
                            int32_t B, const int32_t* m_offsets, int64_t total_drafts,
                            const int32_t* draft_tokens, const sdcp_session_params* params,
                            int32_t* accepted, int32_t* n_out, int32_t* out_tokens, int32_t* status,
-                           void* workspace, size_t workspace_bytes, void* stream, bool pdl) {
+                           void* workspace, size_t workspace_bytes, void* stream, bool pdl,
+                           const sdcp_verify_options* opts = nullptr) {
   int rc = check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens, params,
                         draft_logits);
   if (rc != SDCP_OK) return rc;
@@ -117,9 +119,22 @@ static int verify_sessions(const void* target_logits, const void* draft_logits, 
   if (!accepted || !n_out || !out_tokens || !status) return SDCP_E_INVALID;
   rc = check_workspace(workspace, workspace_bytes, V, B, total_drafts);
   if (rc != SDCP_OK) return rc;
-  const SessIO io = make_io(target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens,
-                            params, accepted, n_out, out_tokens, status, workspace);
+  SessIO io = make_io(target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens,
+                      params, accepted, n_out, out_tokens, status, workspace);
+  if (opts) {
+    io.rng = opts->rng_id;
+    io.session_ids = opts->session_ids;
+  }
   if (launch_sessions(io, dtype, pdl, reinterpret_cast<cudaStream_t>(stream)) != 0) return SDCP_E_LAUNCH;
+  return SDCP_OK;
+}
+
+// Checks of the options of sdcp_verify_batch_ex (NULL: the defaults).
+static int check_options(const sdcp_verify_options* opts) {
+  if (!opts) return SDCP_OK;
+  if (opts->struct_size < sizeof(sdcp_verify_options)) return SDCP_E_INVALID;
+  if (opts->rng_id != SDCP_RNG_PHILOX4X32_10 && opts->rng_id != SDCP_RNG_HMAC_SHA256) return SDCP_E_INVALID;
+  if (opts->rng_id == SDCP_RNG_HMAC_SHA256 && !opts->session_ids) return SDCP_E_INVALID;
   return SDCP_OK;
 }
 
@@ -150,6 +165,26 @@ int sdcp_verify_batch(const void* target_logits, const void* draft_logits, int d
   return verify_sessions(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
                          draft_tokens, params, accepted, n_out, out_tokens, status, workspace,
                          workspace_bytes, stream, true);
+}
+
+int sdcp_verify_batch_ex(const void* target_logits, const void* draft_logits, int dtype, int64_t V,
+                         int32_t B, const int32_t* m_offsets, int64_t total_drafts,
+                         const int32_t* draft_tokens, const sdcp_session_params* params,
+                         int32_t* accepted, int32_t* n_out, int32_t* out_tokens, int32_t* status,
+                         void* workspace, size_t workspace_bytes, const sdcp_verify_options* opts,
+                         void* stream) {
+  int rc = check_common(target_logits, dtype, V, B, m_offsets, total_drafts, draft_tokens, params,
+                        draft_logits);
+  if (rc != SDCP_OK) return rc;
+  rc = check_options(opts);
+  if (rc != SDCP_OK) return rc;
+  if (B > 0 && (!accepted || !n_out || !out_tokens || !status)) return SDCP_E_INVALID;
+  rc = sdcp_verify_rows(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
+                        draft_tokens, params, workspace, workspace_bytes, stream);
+  if (rc != SDCP_OK || B == 0) return rc;
+  return verify_sessions(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
+                         draft_tokens, params, accepted, n_out, out_tokens, status, workspace,
+                         workspace_bytes, stream, true, opts);
 }
 
 int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtype, int64_t V,

@@ -58,6 +58,8 @@ struct SessIO {
   int32_t* out_tokens;
   int32_t* status;
   const uint32_t* error;  // non-zero: a bounded wait of the call gave up
+  uint32_t rng;                // SDCP_RNG_*
+  const uint8_t* session_ids;  // [B][16] session identifiers (SDCP_RNG_HMAC_SHA256)
 };
 
 // Arguments of the row kernel.
@@ -396,6 +398,27 @@ __device__ __forceinline__ float group_excl_scan(const Group& g, float v, float*
   if (l == 31) scratch[w] = incl;
   g.sync();
   float base = 0.f, tot = 0.f;
+  for (int i = 0; i < g.nwarps(); ++i) {
+    if (i == w) base = tot;
+    tot += scratch[i];
+  }
+  *total = tot;
+  return base + ex;
+}
+__device__ __forceinline__ double group_excl_scan_d(const Group& g, double v, double* scratch, double* total) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  double incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (l >= o) incl += t;
+  }
+  double ex = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (l == 0) ex = 0.0;
+  g.sync();
+  if (l == 31) scratch[w] = incl;
+  g.sync();
+  double base = 0.0, tot = 0.0;
   for (int i = 0; i < g.nwarps(); ++i) {
     if (i == w) base = tot;
     tot += scratch[i];

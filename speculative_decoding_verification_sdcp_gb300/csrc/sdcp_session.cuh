@@ -17,6 +17,7 @@
 #pragma once
 
 #include "sdcp_device.cuh"
+#include "sdcp_sha256.cuh"
 
 namespace sdcp {
 
@@ -29,6 +30,7 @@ constexpr int kDrawStages = 2;      // stages of the streamed draw's ring
 constexpr int kKeptW = 128;         // candidates (p's kept tokens) per warp: kept-set draw
 constexpr int kQCutW = 32;          // q's cut-value ids per warp: kept-set draw
 constexpr int kKeptSliceBytes = 65536;  // largest slice of p a CTA scans with plain loads
+#define kNaN64 __longlong_as_double(0x7FF8000000000000ll)  // "the draw could not decide"
 
 // A token whose keptness depends on its rank among the tokens of a cut value (p's or q's).
 struct TieEntry {
@@ -66,9 +68,10 @@ struct SessSmem {
   int tie_p_cand, tie_q_cand;  // id bounds found in this slice (read by the cluster)
   float fscr[2 * 32 + 4];
   long long lscr[2 * 32 + 4];
-  float cta_sum;       // the slice's total weight (read by the cluster)
+  double cta_sum;      // the slice's total weight (read by the cluster)
   long long cta_cnt;   // the slice's tie count (read by the cluster)
-  float owner_base;
+  double owner_base;
+  double dscr[2 * 32 + 4];
   long long owner_pre, owner_carry;
   long long result;    // a tie id found by this CTA (read by the cluster)
   int st, a, draw;
@@ -80,6 +83,24 @@ struct Verdict {
   int st, a;
   bool draw;
 };
+
+// The verifier's random value of session b for 0-based position pos and purpose (0: the
+// acceptance test, 1: the additional token), by the call's generator: Philox with counter
+// (pos, purpose, round, session_tag), or the draft's HMAC-SHA-256 derivation with the
+// session's 16-octet identifier and the 1-based position pos + 1.
+__device__ __forceinline__ double session_uniform(const SessIO& A, int32_t b, const sdcp_session_params& P,
+                                                  uint32_t pos, uint32_t purpose) {
+  if (A.rng == SDCP_RNG_HMAC_SHA256) {
+    const uint8_t* s = A.session_ids + (size_t)16 * (size_t)b;
+    uint32_t sid[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      sid[w] = ((uint32_t)s[4 * w] << 24) | ((uint32_t)s[4 * w + 1] << 16) | ((uint32_t)s[4 * w + 2] << 8) |
+               (uint32_t)s[4 * w + 3];
+    return hmac_uniform(P.seed, sid, P.round, pos + 1u, purpose);
+  }
+  return verifier_uniform(P, pos, purpose);
+}
 
 // A row statistic as the other CTAs of the grid left it in L2 (never a stale L1 line).
 __device__ __forceinline__ RowStat load_stat(const RowStat* p) {
@@ -137,7 +158,7 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
             if (sp.flags & SDCP_ROW_X_KEPT)
               ratio = ex2((sp.dlx - sq.dlx) * c) * __fdiv_rn(sq.s, sp.s);
             ratio = ratio > 1.f ? 1.f : ratio;
-            const double u = verifier_uniform(P, (uint32_t)i, 0u);
+            const double u = session_uniform(A, b, P, (uint32_t)i, 0u);
             rej[h] = !(u < (double)ratio);
           }
         } else {
@@ -340,10 +361,12 @@ __device__ void draw_pass(const SegSlice& sl, SessSmem& sm, const T* prow, const
 
 // One warp walks segments [k0, k1) from cumulative weight `carry`: the smallest id whose
 // cumulative weight exceeds target, else (rounding) the largest id with positive weight seen.
+// Weights and their sums within a segment are fp32; the running total across segments and
+// the comparison with the target are fp64, so long rows keep the position of u * W.
 template <typename T, bool FILT>
 __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p, bool al_q, int V,
-                         const DrawRow& pr, const DrawRow& qr, int k0, int k1, float carry,
-                         float target, bool last_only) {
+                         const DrawRow& pr, const DrawRow& qr, int k0, int k1, double carry,
+                         double target, bool last_only) {
   const int lane = threadIdx.x & 31;
   int lastpos = -1;
   for (int k = k0; k < k1; ++k) {
@@ -364,19 +387,20 @@ __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p,
       const float tv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
       if (lane >= o) incl += tv;
     }
-    const float start = carry + (incl - ls);
+    const double start = carry + (double)(incl - ls);
     int hit = INT_MAX;
-    if (start <= target && target < start + ls) {
-      float cc = start;
+    if (start <= target && target < start + (double)ls) {
+      double cc = start;
 #pragma unroll
       for (int e = 0; e < kEpt; ++e) {
-        cc += wv[e];
+        cc += (double)wv[e];
         if (hit == INT_MAX && wv[e] > 0.f && cc > target) hit = j0 + e;
       }
+      if (hit == INT_MAX) hit = lp;  // the lane's sum reached the target, its steps fell short
     }
     const int found = __reduce_min_sync(0xFFFFFFFFu, hit);
-    if (found != INT_MAX) return found;
-    carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (found != INT_MAX && found >= 0) return found;
+    carry += (double)__shfl_sync(0xFFFFFFFFu, incl, 31);
   }
   return lastpos;
 }
@@ -388,60 +412,61 @@ __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p,
 // ---------------------------------------------------------------------------------
 
 // Returns W (the same in every CTA), or NaN when some CTA of the cluster flagged its pass
-// as unusable (sm.overflow).  Tie ids come from the CTAs' candidates when `ties`.
+// as unusable (sm.overflow).  Tie ids come from the CTAs' candidates when `ties`.  Segment
+// sums are fp32; every sum across segments, slices and CTAs is fp64.
 template <typename T, bool FILT>
-__device__ float locate_and_walk(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+__device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                               const SegSlice& sl, const T* prow, const T* qrow, bool residual,
                                               bool al_p, bool al_q, int V, DrawRow pr, DrawRow qr,
                                               bool pp, bool qp, double u1, int32_t* out) {
   const int t = threadIdx.x, w = t >> 5, lane = t & 31;
   const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
   const int gpt = (sl.ngrp + g.nthreads - 1) / g.nthreads;
-  float loc = 0.f;
+  double loc = 0.0;
   for (int i = 0; i < gpt; ++i) {
     const int k = t * gpt + i;
-    if (k < sl.ngrp) loc += sm.seg[k];
+    if (k < sl.ngrp) loc += (double)sm.seg[k];
   }
-  float Wc;
-  const float pre = group_excl_scan(g, loc, sm.fscr, &Wc);
+  double Wc;
+  const double pre = group_excl_scan_d(g, loc, sm.dscr, &Wc);
   if (t == 0) { sm.cta_sum = Wc; sm.cta_ovf = sm.overflow; }
   cluster.sync();
-  float W = 0.f;
+  double W = 0.0;
   int owner = -1, lastr = -1, tp_id = INT_MAX, tq_id = INT_MAX, bad = 0;
-  float obase = 0.f;
+  double obase = 0.0;
   for (unsigned r = 0; r < C; ++r) {
-    const float sr = *cluster.map_shared_rank(&sm.cta_sum, r);
-    if (sr > 0.f) lastr = (int)r;
+    const double sr = *cluster.map_shared_rank(&sm.cta_sum, r);
+    if (sr > 0.0) lastr = (int)r;
     W += sr;
     tp_id = min(tp_id, *cluster.map_shared_rank(&sm.tie_p_cand, r));
     tq_id = min(tq_id, *cluster.map_shared_rank(&sm.tie_q_cand, r));
     bad |= *cluster.map_shared_rank(&sm.cta_ovf, r);
   }
-  const float target = (float)(u1 * (double)W);
+  const double target = u1 * W;
   {
-    float acc = 0.f;
+    double acc = 0.0;
     for (unsigned r = 0; r < C; ++r) {
-      const float sr = *cluster.map_shared_rank(&sm.cta_sum, r);
-      if (owner < 0 && sr > 0.f && acc <= target && target < acc + sr) { owner = (int)r; obase = acc; }
+      const double sr = *cluster.map_shared_rank(&sm.cta_sum, r);
+      if (owner < 0 && sr > 0.0 && acc <= target && target < acc + sr) { owner = (int)r; obase = acc; }
       acc += sr;
     }
   }
   cluster.sync();  // every CTA has read the slice totals
-  if (bad) return __int_as_float(0x7FC00000);
-  if (!(W > 0.f)) return W;
+  if (bad) return kNaN64;
+  if (!(W > 0.0)) return W;
   const bool mine = (owner == (int)rank) || (owner < 0 && lastr == (int)rank);
   if (!mine) return W;
   pr.tie = pp ? tp_id : INT_MAX;
   qr.tie = qp ? tq_id : INT_MAX;
   long long cand = LLONG_MAX, lastg = -1;
-  float cbase = 0.f;
+  double cbase = 0.0;
   if (owner >= 0) {
-    float bsum = obase + pre;
+    double bsum = obase + pre;
     for (int i = 0; i < gpt; ++i) {
       const int k = t * gpt + i;
       if (k >= sl.ngrp) break;
-      const float sk = sm.seg[k];
-      if (cand == LLONG_MAX && sk > 0.f && bsum <= target && target < bsum + sk) { cand = k; cbase = bsum; }
+      const double sk = (double)sm.seg[k];
+      if (cand == LLONG_MAX && sk > 0.0 && bsum <= target && target < bsum + sk) { cand = k; cbase = bsum; }
       bsum += sk;
     }
   }
@@ -460,7 +485,7 @@ __device__ float locate_and_walk(cg::cluster_group& cluster, const Group& g, Ses
                                sl.grp_hi((int)og), sm.owner_base, target, false);
     } else {  // u * W rounded up to the end: the largest id with positive weight
       tok = draw_walk<T, FILT>(prow, qrow, residual, al_p, al_q, V, pr, qr, sl.grp_lo((int)lg),
-                               sl.grp_hi((int)lg), 0.f, 0.f, true);
+                               sl.grp_hi((int)lg), 0.0, 0.0, true);
     }
     if (lane == 0) *out = tok;
   }
@@ -576,7 +601,7 @@ static __device__ bool resolve_ties(cg::cluster_group& cluster, const Group& g, 
 
 // Without cut-value tokens to rank: every token's weight is known during the pass.
 template <typename T, bool FILT>
-__device__ float draw_token(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+__device__ double draw_token(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                          const T* prow, const T* qrow, bool residual, bool al_p,
                                          bool al_q, int V, const DrawRow& pr, const DrawRow& qr,
                                          double u1, int32_t* out) {
@@ -591,7 +616,7 @@ __device__ float draw_token(cg::cluster_group& cluster, const Group& g, SessSmem
 
 // A cut inside a value (p's, q's or both), in one pass; NaN when a list overflowed.
 template <typename T>
-__device__ float draw_token_ties(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+__device__ double draw_token_ties(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                               const T* prow, const T* qrow, bool residual, bool al_p,
                                               bool al_q, int V, const DrawRow& pr, const DrawRow& qr,
                                               int np_cut, int nq_cut, double u1, int32_t* out) {
@@ -651,7 +676,7 @@ __device__ float draw_token_ties(cg::cluster_group& cluster, const Group& g, Ses
     }
   }
   g.sync();
-  if (!resolve_ties(cluster, g, sm, sl, 1, residual, np_cut, nq_cut)) return __int_as_float(0x7FC00000);
+  if (!resolve_ties(cluster, g, sm, sl, 1, residual, np_cut, nq_cut)) return kNaN64;
   return locate_and_walk<T, true>(cluster, g, sm, sl, prow, qrow, residual, al_p, al_q, V, pr, qr, pp, qp,
                                   u1, out);
 }
@@ -674,7 +699,7 @@ __device__ __forceinline__ bool stream_ok(int V, unsigned C, unsigned rank, bool
 }
 
 template <typename T, bool FILT, bool TIES>
-__device__ float draw_stream(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
+__device__ double draw_stream(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                           unsigned char* ring, const T* prow, const T* qrow, bool residual,
                                           int V, const DrawRow& pr, const DrawRow& qr, int np_cut,
                                           int nq_cut, double u1, int32_t* out) {
@@ -789,7 +814,7 @@ __device__ float draw_stream(cg::cluster_group& cluster, const Group& g, SessSme
   }
   if (t == 0) sm.ring_uses = use0 + (uint32_t)nst;
   g.sync();
-  if (TIES && !resolve_ties(cluster, g, sm, sl, nst, residual, np_cut, nq_cut)) return __int_as_float(0x7FC00000);
+  if (TIES && !resolve_ties(cluster, g, sm, sl, nst, residual, np_cut, nq_cut)) return kNaN64;
   const bool al_p = ((uintptr_t)prow & 15u) == 0, al_q = ((uintptr_t)qrow & 15u) == 0;
   return locate_and_walk<T, FILT || TIES>(cluster, g, sm, sl, prow, qrow, residual, al_p, al_q, V, pr, qr,
                                           pp, qp, u1, out);
@@ -963,7 +988,7 @@ __device__ __forceinline__ int kth_qcut(const KeptSmem& K, long long k) {
 }
 
 template <typename T>
-__device__ float draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem& sm, const T* prow,
+__device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem& sm, const T* prow,
                            const T* qrow, bool residual, bool al_p, bool al_q, int V, DrawRow pr, DrawRow qr,
                            int np_cut, int nq_cut, double u1, int32_t* out) {
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -1090,31 +1115,31 @@ __device__ float draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem&
     sm.cta_ovf = K.cta_ovf;
   }
   cluster.sync();
-  float W = 0.f, acc = 0.f, cbase = 0.f;
+  double W = 0.0, acc = 0.0, cbase = 0.0;
   int owner = -1, lastr = -1;
   for (unsigned r = 0; r < C; ++r) {
     bad |= *cluster.map_shared_rank(&sm.cta_ovf, r) != 0;
-    const float sr = *cluster.map_shared_rank(&sm.cta_sum, r);
-    if (sr > 0.f) lastr = (int)r;
+    const double sr = *cluster.map_shared_rank(&sm.cta_sum, r);
+    if (sr > 0.0) lastr = (int)r;
     W += sr;
   }
-  const float target = (float)(u1 * (double)W);
+  const double target = u1 * W;
   for (unsigned r = 0; r < C; ++r) {
-    const float sr = *cluster.map_shared_rank(&sm.cta_sum, r);
-    if (sr > 0.f && acc <= target) { owner = (int)r; cbase = acc; }
+    const double sr = *cluster.map_shared_rank(&sm.cta_sum, r);
+    if (sr > 0.0 && acc <= target) { owner = (int)r; cbase = acc; }
     acc += sr;
   }
   cluster.sync();  // every CTA has read the slice totals
-  if (bad) return __int_as_float(0x7FC00000);
-  if (!(W > 0.f)) return W;
-  if (owner < 0) { owner = lastr; cbase = 0.f; }
+  if (bad) return kNaN64;
+  if (!(W > 0.0)) return W;
+  if (owner < 0) { owner = lastr; cbase = 0.0; }
   if (owner != (int)rank) return W;
   // the owner: the last candidate with weight whose interval starts at or below the target
   // (a target past every interval, from rounding, takes the last token with weight)
   int best = -1;
   for (int i = lane; i < nc; i += 32) {
     const float x = K.r[w][i];
-    if (x > 0.f && cbase + K.wbase[w] + K.pre[w][i] <= target) best = i;
+    if (x > 0.f && cbase + (double)K.wbase[w] + (double)K.pre[w][i] <= target) best = i;
   }
   const int wb = __reduce_max_sync(0xFFFFFFFFu, (unsigned)(best + 1)) - 1;
   int anyw = -1;
@@ -1161,13 +1186,13 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
   qr.thr = filt_q ? key_value(sq.thr_key) : -INFINITY;
   pr.tie = INT_MAX;
   qr.tie = INT_MAX;
-  const double u1 = verifier_uniform(P, (uint32_t)a, 1u);
+  const double u1 = session_uniform(A, b, P, (uint32_t)a, 1u);
   int32_t* out = A.out_tokens + off0 + b + a;
   for (int attempt = 0; attempt < 2; ++attempt) {
     const bool filt = filt_p || (residual && filt_q);
     const int np_cut = sp.thr_n, nq_cut = residual ? sq.thr_n : INT_MAX;
     const bool ties = np_cut != INT_MAX || nq_cut != INT_MAX;
-    float W = __int_as_float(0x7FC00000);
+    double W = kNaN64;
     // first choice where p has a cut and the slices are short: weigh p's kept tokens only
     if (filt_p && (long long)((V + (int)C - 1) / (int)C) * (long long)sizeof(T) <= kKeptSliceBytes)
       W = draw_kept<T>(cluster, g, sm, trow, drow, residual, al_p, al_q, V, pr, qr, np_cut, nq_cut, u1, out);

@@ -28,6 +28,27 @@ PARAMS_DTYPE = np.dtype([("rule_id", "<u4"), ("temperature_milli", "<u4"), ("top
 ROW_STAT_DTYPE = np.dtype([("lmax", "<f4"), ("log_s", "<f4"), ("lp_x", "<f4"), ("argmax", "<i4"),
                            ("kept", "<i4"), ("thr_key", "<u4"), ("thr_n", "<i4"), ("flags", "<u4")])
 
+# random generators of the acceptance step
+RNG_PHILOX4X32_10, RNG_HMAC_SHA256 = 0, 1
+# actions of a verdict, and the contract's "no self_load"
+ACTION_NONE, ACTION_CONTINUE, ACTION_REDUCE, ACTION_SWITCH = -1, 0, 1, 2
+ACTION_SELF_DECODE, ACTION_FINISH, ACTION_FAIL = 3, 4, 5
+NO_SELF_LOAD = 0xFFFFFFFF
+# sdcp_commit_params (48 bytes) and sdcp_session_state (64 bytes)
+COMMIT_PARAMS_DTYPE = np.dtype([("max_new", "<u4"), ("stop_offset", "<u4"), ("stop_count", "<u4"),
+                                ("m_max", "<u4"), ("low_rounds", "<u4"), ("low_ratio", "<u4"),
+                                ("self_load", "<u4"), ("fallback_len", "<u4"), ("fallback", "u1", (8,)),
+                                ("m_restore", "<u4"), ("reserved", "<u4")])
+STATE_DTYPE = np.dtype([("digest", "u1", (32,)), ("committed", "<u4"), ("c", "<u4"), ("g", "<u4"),
+                        ("j", "<u4"), ("m_cap", "<u4"), ("reserved", "<u4", (3,))])
+assert COMMIT_PARAMS_DTYPE.itemsize == 48 and STATE_DTYPE.itemsize == 64
+
+
+class VerifyOptions(ctypes.Structure):
+    """sdcp_verify_options."""
+    _fields_ = [("struct_size", ctypes.c_uint32), ("rng_id", ctypes.c_uint32),
+                ("session_ids", ctypes.c_void_p)]
+
 
 class SdcpError(RuntimeError):
     pass
@@ -55,6 +76,11 @@ def _load():
     L.sdcp_verify_batch_noalloc.restype = ctypes.c_int
     L.sdcp_row_stats.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, vp, sz, vp]
     L.sdcp_row_stats.restype = ctypes.c_int
+    L.sdcp_verify_batch_ex.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp, vp, vp,
+                                       vp, vp, sz, ctypes.POINTER(VerifyOptions), vp]
+    L.sdcp_verify_batch_ex.restype = ctypes.c_int
+    L.sdcp_commit_batch.argtypes = [i32, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_uint32, vp, vp]
+    L.sdcp_commit_batch.restype = ctypes.c_int
     L.sdcp_split_sessions.argtypes = [vp, vp, i32, i32, vp]
     L.sdcp_split_sessions.restype = ctypes.c_int
     L.sdcp_strerror.argtypes = [ctypes.c_int]
@@ -131,6 +157,39 @@ def sdcp_verify_batch(target_logits, draft_logits, m_offsets, total_drafts, draf
                                    _ptr(params_dev), _ptr(accepted), _ptr(n_out), _ptr(out_tokens),
                                    _ptr(status), _ptr(workspace), workspace.numel(), s)
     _check(rc, "sdcp_verify_batch")
+
+
+def sdcp_verify_batch_ex(target_logits, draft_logits, m_offsets, total_drafts, draft_tokens,
+                         params_dev, accepted, n_out, out_tokens, status, workspace,
+                         rng_id=RNG_PHILOX4X32_10, session_ids=None, stream=None):
+    """sdcp_verify_batch with the random generator chosen by rng_id (session_ids: a device
+    uint8 tensor [B, 16] of session identifiers, for the HMAC-SHA-256 generator)."""
+    V = target_logits.shape[1]
+    B = accepted.shape[0]
+    s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
+    opts = VerifyOptions(ctypes.sizeof(VerifyOptions), int(rng_id),
+                         None if session_ids is None else session_ids.data_ptr())
+    with _on(target_logits):
+        rc = lib.sdcp_verify_batch_ex(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits),
+                                      V, B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
+                                      _ptr(params_dev), _ptr(accepted), _ptr(n_out), _ptr(out_tokens),
+                                      _ptr(status), _ptr(workspace), workspace.numel(),
+                                      ctypes.byref(opts), s)
+    _check(rc, "sdcp_verify_batch_ex")
+
+
+def sdcp_commit_batch(m_offsets, accepted, n_out, out_tokens, status, cparams_dev, stop_tokens,
+                      state_dev, load_percent, action, stream=None):
+    """The commit step after acceptance (truncation, digest chain, control) on device tensors:
+    cparams_dev / state_dev are uint8 tensors holding COMMIT_PARAMS_DTYPE / STATE_DTYPE
+    records; n_out, out_tokens and state_dev are updated in place."""
+    B = accepted.shape[0]
+    s = _stream_handle(accepted.device) if stream is None else ctypes.c_void_p(stream)
+    with _on(accepted):
+        rc = lib.sdcp_commit_batch(B, _ptr(m_offsets), _ptr(accepted), _ptr(n_out), _ptr(out_tokens),
+                                   _ptr(status), _ptr(cparams_dev), _ptr(stop_tokens), _ptr(state_dev),
+                                   int(load_percent), _ptr(action), s)
+    _check(rc, "sdcp_commit_batch")
 
 
 NOALLOC_SCRATCH_BYTES = 2 << 20
@@ -212,10 +271,16 @@ class Verifier:
         self.status = torch.empty(B, dtype=torch.int32, device=self.device)
         self.workspace = alloc_workspace(V, B, self.total, self.device)
 
-    def __call__(self, target, draft, m_offsets, draft_tokens, params_dev, stream=None):
-        sdcp_verify_batch(target, draft, m_offsets, self.total, draft_tokens, params_dev,
-                          self.accepted, self.n_out, self.out_tokens, self.status,
-                          self.workspace, stream)
+    def __call__(self, target, draft, m_offsets, draft_tokens, params_dev, stream=None,
+                 rng_id=RNG_PHILOX4X32_10, session_ids=None):
+        if rng_id == RNG_PHILOX4X32_10 and session_ids is None:
+            sdcp_verify_batch(target, draft, m_offsets, self.total, draft_tokens, params_dev,
+                              self.accepted, self.n_out, self.out_tokens, self.status,
+                              self.workspace, stream)
+        else:
+            sdcp_verify_batch_ex(target, draft, m_offsets, self.total, draft_tokens, params_dev,
+                                 self.accepted, self.n_out, self.out_tokens, self.status,
+                                 self.workspace, rng_id, session_ids, stream)
         return self.accepted, self.n_out, self.out_tokens, self.status
 
     def phases(self, target, draft, m_offsets, draft_tokens, params_dev, ev_mid=None):

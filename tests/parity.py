@@ -63,6 +63,10 @@ def session_arrays(T, D, off, x, params, b):
             np.ascontiguousarray(x[o0:o1], dtype=np.int32), params[b:b + 1])
 
 
+def _sid(session_ids, b):
+    return None if session_ids is None else session_ids[b:b + 1]
+
+
 def session_outputs(got, off, b):
     o0, o1 = int(off[b]), int(off[b + 1])
     return {"status": got["status"][b:b + 1], "accepted": got["accepted"][b:b + 1],
@@ -121,7 +125,7 @@ def _row_margin(info):
                abs(info.topp_cum_before - info.topp_target)) / info.topp_target
 
 
-def _forced_session(T, D, off, x, params, b, gs):
+def _forced_session(T, D, off, x, params, b, gs, session_ids=None):
     """The oracle on session b alone with the GPU's top-p crossings at the session's
     boundary rows (each checked to lie in its band)."""
     B = params.shape[0]
@@ -143,10 +147,11 @@ def _forced_session(T, D, off, x, params, b, gs):
         lo, hi = topp_band(logits, tm, k, p)
         assert lo <= n <= hi, ("session %d row %d: GPU crossing %d outside the band [%d, %d]" % (b, r, n, lo, hi))
         force[j] = n
-    return args, force, oracle.verify_batch(*args, force_kept=force)
+    return args, force, oracle.verify_batch(*args, force_kept=force, session_ids=_sid(session_ids, b))
 
 
-def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None, force=None):
+def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None, force=None,
+                     session_ids=None):
     """One session; adds to counts; raises AssertionError on a real disagreement.  force:
     the top-p crossings ref was computed with (None: as defined)."""
     det = ref["detail"]
@@ -167,9 +172,10 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
         # the oracle under one of the band's two ends
         mine = session_outputs(got, off, b)
         if gs is not None:
-            args, force2, r2 = _forced_session(T, D, off, x, params, b, gs)
+            args, force2, r2 = _forced_session(T, D, off, x, params, b, gs, session_ids)
             c2 = {"exact": 0, "accept_boundary": 0, "draw_boundary": 0, "topp_boundary": 0}
-            _compare_session(mine, r2, *args, 0, c2, topp_ok=False, force=force2)
+            _compare_session(mine, r2, *args, 0, c2, topp_ok=False, force=force2,
+                             session_ids=_sid(session_ids, b))
             counts["topp_boundary"] += 1
             return
         args = session_arrays(T, D, off, x, params, b)
@@ -177,9 +183,10 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
         for shift in (-BOUNDARY, BOUNDARY):
             c2 = {"exact": 0, "accept_boundary": 0, "draw_boundary": 0, "topp_boundary": 0}
             with oracle.topp_shift(shift):
-                r2 = oracle.verify_batch(*args)
+                r2 = oracle.verify_batch(*args, session_ids=_sid(session_ids, b))
                 try:
-                    _compare_session(mine, r2, *args, 0, c2, topp_ok=False)
+                    _compare_session(mine, r2, *args, 0, c2, topp_ok=False,
+                                     session_ids=_sid(session_ids, b))
                 except AssertionError as e:
                     errs.append(str(e))
                     continue
@@ -211,7 +218,7 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
                           ref["out_tokens"][o0 + b + a + 1:o1 + b + 1])
 
 
-def compare_verdicts(got, ref, T, D, off, x, params, gs=None):
+def compare_verdicts(got, ref, T, D, off, x, params, gs=None, session_ids=None):
     """Returns a dict of counts; raises AssertionError on a real disagreement.  gs: the
     GPU's row statistics of the same batch (sdcp_row_stats), used where a top-p crossing
     lies within rounding of P."""
@@ -220,7 +227,8 @@ def compare_verdicts(got, ref, T, D, off, x, params, gs=None):
               "topp_boundary": 0}
     assert np.array_equal(got["status"], ref["status"]), (got["status"], ref["status"])
     for b in range(B):
-        _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok=True, gs=gs)
+        _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok=True, gs=gs,
+                         session_ids=session_ids)
     return counts
 
 
