@@ -412,7 +412,7 @@ def run_ours(args, dist: Dist):
         cpu = {"value": toks / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "%d sessions of the same batch (%d oracle calls of %d sessions, %.1f s, fp64 C with OpenMP)" % (
                    sess, calls, min(batch.B, cores), secs)}
-    head_launches = 2 * K
+    head_launches = 2 * K  # the row kernel and the session kernel of every step
     del head["_batch"], head["_ver"]
     torch.cuda.empty_cache()
 

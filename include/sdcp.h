@@ -63,6 +63,15 @@ extern "C" {
 /* ---- acceptance rules: SDCP Section 10.2.2 registry ------------------------------ */
 #define SDCP_RULE_GREEDY 1              /* Rule 1 */
 #define SDCP_RULE_SPECULATIVE_SAMPLING 2 /* Rule 2 */
+/* A private-use rule (Section 10.2 keeps ids 192-255 for private use): the relaxed rule of
+ * "Inference: KV Cache, Batching, Speculative Decoding" (section on variants of the
+ * acceptance rule: accept if the token is in the target's top-k).  Acceptance test: x[i]
+ * lies in the kept set of p[i], the target distribution after the session's sampling profile
+ * (top_k = k makes it "in the target's top-k"), with a finite logit.  Additional token: a
+ * draw from p[a] (purpose 1) at the first rejection, or from p[M+1] when all M are accepted;
+ * argmax at temperature 0.  The proposal carries tokens only: draft rows are never read.  It
+ * does NOT preserve the target distribution, and needs no trust in a drafter's q. */
+#define SDCP_RULE_RELAXED_TOP_K 192
 
 /* ---- return codes ---------------------------------------------------------------- */
 #define SDCP_OK           0
@@ -123,8 +132,10 @@ size_t sdcp_workspace_bytes(int64_t V, int32_t B, int64_t total_drafts);
  *                is not 16-byte aligned are read with narrower loads at their ends.
  * B              number of sessions, >= 0 (B = 0 launches nothing).
  * m_offsets      device, [B+1] int32, m_offsets[0] = 0, non-decreasing,
- *                m_offsets[B] = total_drafts; inconsistent values give SDCP_S_BAD_PARAMS
- *                to the sessions they touch, never an out-of-range access.
+ *                m_offsets[B] = total_drafts.  A session whose own pair m_offsets[b],
+ *                m_offsets[b+1] is out of order or out of range gets SDCP_S_BAD_PARAMS;
+ *                offsets out of order elsewhere leave the results of the sessions they
+ *                overlap unspecified.  Never an out-of-range access.
  * total_drafts   host copy of m_offsets[B] (sizes the launch without a device read).
  * draft_tokens   device, [total_drafts] int32, the proposed tokens x[i].
  * params         device, [B] sdcp_session_params.

@@ -46,7 +46,8 @@ DETAIL_DTYPE = np.dtype([
     ("u0", "<f8", (MMAX,)), ("ratio", "<f8", (MMAX,)), ("log_p", "<f8", (MMAX,)),
     ("log_q", "<f8", (MMAX,)), ("topp_margin", "<f8")])
 
-EXTRA_ARGMAX, EXTRA_RESIDUAL, EXTRA_BONUS, EXTRA_RESIDUAL_AS_P = 1, 2, 3, 4
+EXTRA_ARGMAX, EXTRA_RESIDUAL, EXTRA_BONUS, EXTRA_RESIDUAL_AS_P, EXTRA_FROM_P = 1, 2, 3, 4, 5
+RULE_GREEDY, RULE_SPECULATIVE_SAMPLING, RULE_RELAXED_TOP_K = 1, 2, 192
 
 _lib = None
 

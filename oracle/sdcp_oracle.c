@@ -58,6 +58,15 @@ enum { ORC_F32 = 0, ORC_BF16 = 1 };
 enum { ORC_OK = 0, ORC_BAD_PROPOSAL = 1, ORC_LIMIT = 2, ORC_BAD_PARAMS = 3,
        ORC_Q_UNAVAILABLE = 4 };
 enum { ORC_MMAX = 64 };
+/* A private-use acceptance rule (the draft's registry keeps 192-255 for private use, Section
+   10.2): the relaxed rule of "Inference: KV Cache, Batching, Speculative Decoding", section
+   on variants of the acceptance rule ("accept if the token is in the target's top-k").
+   Acceptance test: x[i] lies in the kept set of p[i] (the target distribution after the
+   session's sampling profile; top_k = k gives "in the target's top-k") with a finite logit.
+   Additional token: a draw from p[a] (purpose 1), whether at the first rejection or after
+   all M (argmax at temperature 0).  A proposal carries tokens only (no q).  It does not
+   preserve the target distribution and needs no trust in a drafter's q. */
+enum { ORC_RULE_RELAXED = 192 };
 
 typedef struct {
   uint32_t rule_id, temperature_milli, top_k, top_p_milli;
@@ -79,7 +88,7 @@ typedef struct {
 
 /* Per-session record of every decision, so that a disagreement can be classified. */
 typedef struct {
-  int32_t status, a, n_out, extra_mode; /* extra_mode: 0 none, 1 argmax, 2 residual, 3 bonus, 4 residual fell back to p */
+  int32_t status, a, n_out, extra_mode; /* extra_mode: 0 none, 1 argmax, 2 residual, 3 bonus, 4 residual fell back to p, 5 draw from p at a rejection (relaxed rule) */
   int32_t extra_token, extra_pos, m, pad;
   double u1, W, c_lo, c_hi;          /* draw: uniform, total weight, C_{j-1}, C_j */
   double u0[ORC_MMAX];               /* acceptance uniforms at evaluated positions */
@@ -417,7 +426,7 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
   int64_t M = off1 - off0;
   det->m = (int32_t)M;
   int st = ORC_OK;
-  if (prm->rule_id != 1 && prm->rule_id != 2) st = ORC_BAD_PARAMS;
+  if (prm->rule_id != 1 && prm->rule_id != 2 && prm->rule_id != ORC_RULE_RELAXED) st = ORC_BAD_PARAMS;
   else if (prm->top_p_milli > 1000) st = ORC_BAD_PARAMS;
   else if (!offsets_ok) st = ORC_BAD_PARAMS;
   else if (M < 1 || M > ORC_MMAX) st = ORC_LIMIT;
@@ -427,6 +436,7 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
       if (x[off0 + i] < 0 || x[off0 + i] >= V) { st = ORC_BAD_PROPOSAL; break; }
   }
   int rule2 = (prm->rule_id == 2);
+  int relaxed = (prm->rule_id == ORC_RULE_RELAXED);
   uint32_t tm = prm->temperature_milli;
 #define TROW(i) ((const char*)T + (size_t)(off0 + b + (i)) * (size_t)V * esz)
 #define DROW(i) ((const char*)D + (size_t)(off0 + (i)) * (size_t)V * esz)
@@ -436,14 +446,15 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
 #define FD(i) (force ? (int64_t)force[R_T + off0 + (i)] : -1)
 
   /* Every scored row is formed before any draw: p for the M+1 target rows, q for the
-     M draft rows (Rule 2).  Rule 1 needs only the argmax of the raw scores. */
+     M draft rows (Rule 2).  Rule 1 needs only the argmax of the raw scores; the relaxed
+     rule needs p's kept sets. */
   orc_row_info* pin = NULL; orc_row_info* qin = NULL;
   uint8_t** pk = NULL; uint8_t** qk = NULL;
   if (st == ORC_OK) {
     pin = (orc_row_info*)calloc((size_t)(M + 1), sizeof(orc_row_info));
     pk = (uint8_t**)calloc((size_t)(M + 1), sizeof(uint8_t*));
     for (int64_t i = 0; i <= M && st == ORC_OK; ++i) {
-      if (rule2) {
+      if (rule2 || relaxed) {
         pk[i] = (uint8_t*)malloc((size_t)V);
         if (row_dist_impl(TROW(i), dtype, V, tm, prm->top_k, prm->top_p_milli, NULL,
                           pk[i], &pin[i], FT(i)))
@@ -476,7 +487,19 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
 
   int64_t a = 0;
   int32_t extra = -1;
-  if (st == ORC_OK && !rule2) {
+  if (st == ORC_OK && relaxed) {
+    /* The relaxed rule: accept while x_i is in the kept set of p_i (finite logit); the
+       additional token is a draw from p_a. */
+    while (a < M && pk[a][x[off0 + a]] && logit_at(TROW(a), dtype, x[off0 + a]) != -INFINITY) ++a;
+    double* pa = (double*)malloc(sizeof(double) * (size_t)V);
+    double* C = (double*)malloc(sizeof(double) * (size_t)V);
+    row_dist_impl(TROW(a), dtype, V, tm, prm->top_k, prm->top_p_milli, pa, NULL, NULL, FT(a));
+    double u1 = verifier_uniform(prm, sid, (uint32_t)a, 1);
+    det->u1 = u1;
+    extra = draw_from(pa, NULL, V, u1, C, &det->W, &det->c_lo, &det->c_hi);
+    det->extra_mode = (a < M) ? 5 : 3;
+    free(pa); free(C);
+  } else if (st == ORC_OK && !rule2) {
     /* Rule 1: accept while x_i is the argmax of target row i; emit argmax of row a. */
     while (a < M && x[off0 + a] == pin[a].argmax) ++a;
     extra = pin[a].argmax;

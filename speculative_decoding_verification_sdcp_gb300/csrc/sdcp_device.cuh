@@ -405,27 +405,6 @@ __device__ __forceinline__ float group_excl_scan(const Group& g, float v, float*
   *total = tot;
   return base + ex;
 }
-__device__ __forceinline__ double group_excl_scan_d(const Group& g, double v, double* scratch, double* total) {
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  double incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (l >= o) incl += t;
-  }
-  double ex = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-  if (l == 0) ex = 0.0;
-  g.sync();
-  if (l == 31) scratch[w] = incl;
-  g.sync();
-  double base = 0.0, tot = 0.0;
-  for (int i = 0; i < g.nwarps(); ++i) {
-    if (i == w) base = tot;
-    tot += scratch[i];
-  }
-  *total = tot;
-  return base + ex;
-}
 __device__ __forceinline__ long long group_excl_scan_ll(const Group& g, long long v, long long* scratch,
                                                         long long* total) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;

@@ -83,12 +83,21 @@ struct RowShared {
 // Per-thread accumulation.  Every row keeps the running maximum fm (max.NaN, so a NaN
 // poisons it); ARGMAX rows also keep the smallest id holding fm (float equality, so -0 and
 // +0 tie and go to the smaller id); SUM rows keep s = sum exp((l - fm) * 1000/T), the sum
-// being rescaled whenever fm grows (online softmax).
+// being rescaled whenever fm grows (online softmax).  The sum is compensated (Kahan: one
+// correction term sc per thread, added once per vector), so a thread's thousands of terms
+// leave S with about one rounding of relative error, not one per term.
 // --------------------------------------------------------------------------------------
 struct ThreadAcc {
-  float fm, fmc, s;  // fmc = fm * c
+  float fm, fmc, s, sc;  // fmc = fm * c; sc: the compensation of s (s - sc is the sum)
   long long amax;
-  __device__ __forceinline__ void reset() { fm = -INFINITY; fmc = -INFINITY; s = 0.f; amax = LLONG_MAX; }
+  __device__ __forceinline__ void reset() { fm = -INFINITY; fmc = -INFINITY; s = 0.f; sc = 0.f; amax = LLONG_MAX; }
+  __device__ __forceinline__ void add(float t) {  // s += t, compensated
+    const float y = t - sc;
+    const float z = s + y;
+    sc = (z - s) - y;
+    s = z;
+  }
+  __device__ __forceinline__ void rescale(float f) { s *= f; sc *= f; }
 };
 
 template <bool ARGMAX, bool SUM>
@@ -96,12 +105,15 @@ __device__ __forceinline__ void acc_element(ThreadAcc& a, uint32_t bits, long lo
   const float v = __uint_as_float(bits);
   const float nm = fmax_nan(a.fm, v);
   if (!(nm == a.fm)) {  // grew, or became NaN
-    if (SUM) a.s = (a.fm == -INFINITY) ? 0.f : a.s * ex2(a.fmc - nm * c);
+    if (SUM) {
+      if (a.fm == -INFINITY) { a.s = 0.f; a.sc = 0.f; }
+      else a.rescale(ex2(a.fmc - nm * c));
+    }
     if (ARGMAX) a.amax = id;
     a.fm = nm;
     a.fmc = nm * c;
   }
-  if (SUM && a.fm != -INFINITY) a.s += ex2(fmaf(v, c, -a.fmc));
+  if (SUM && a.fm != -INFINITY) a.add(ex2(fmaf(v, c, -a.fmc)));
 }
 
 // Maximum of one 16-byte vector, NaN-propagating (bf16: three packed bf16x2 max.NaN).
@@ -131,7 +143,10 @@ __device__ __forceinline__ float acc_vector(ThreadAcc& a, const uint4& q, long l
   const float vm = vec_max(q, T());
   const float nm = fmax_nan(a.fm, vm);
   if (!(nm == a.fm)) {  // the maximum grew (or a NaN arrived): rare after the first vectors
-    if (SUM) a.s = (a.fm == -INFINITY) ? 0.f : a.s * ex2(a.fmc - nm * c);
+    if (SUM) {
+      if (a.fm == -INFINITY) { a.s = 0.f; a.sc = 0.f; }
+      else a.rescale(ex2(a.fmc - nm * c));
+    }
     if (ARGMAX) {
       int first = E - 1;
 #pragma unroll
@@ -145,7 +160,7 @@ __device__ __forceinline__ float acc_vector(ThreadAcc& a, const uint4& q, long l
     float t = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) t += ex2(fmaf(v[e], c, -a.fmc));
-    a.s += t;
+    a.add(t);
   }
   return vm;
 }
@@ -320,7 +335,7 @@ __device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, in
   tok_idx = is_target ? row_id - b : row_id - R_T;
   x.has_x = (pos >= 0 && pos < M && tok_idx >= 0 && tok_idx < A.io.total);
   const bool params_ok = (P.top_p_milli <= 1000u);
-  const bool session_ok = params_ok && (P.rule_id == 1u || P.rule_id == 2u) && M >= 1 &&
+  const bool session_ok = params_ok && (P.rule_id == 1u || P.rule_id == 2u || P.rule_id == SDCP_RULE_RELAXED_TOP_K) && M >= 1 &&
                           M <= SDCP_MAX_M && off0 >= 0 && off1 <= A.io.total;
   bool want_argmax, want_profile;
   if (A.stats_mode) {
@@ -329,9 +344,10 @@ __device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, in
     want_profile = true;
   } else {
     const bool rule2 = (P.rule_id == 2u);
+    const bool profiled = rule2 || P.rule_id == SDCP_RULE_RELAXED_TOP_K;  // p after the profile
     skip = !session_ok || (!is_target && !rule2) || (!is_target && A.io.draft == nullptr);
-    want_argmax = !rule2 || P.temperature_milli == 0u;
-    want_profile = rule2 && P.temperature_milli != 0u;
+    want_argmax = !profiled || P.temperature_milli == 0u;
+    want_profile = profiled && P.temperature_milli != 0u;
   }
   const uint32_t tm = P.temperature_milli;
   x.top_k = P.top_k;
@@ -480,8 +496,16 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
   const int bpl = (nb + 31) >> 5;
   const int d0 = min(nb, l * bpl), d1 = min(nb, d0 + bpl);
   auto e_of = [&](int d) { return ex2((key_value((top16 - (uint32_t)d) << 16) - lmax) * x.c); };
+  // masses are summed with compensation (Kahan): a lane adds up to 64 bins, and the kept
+  // mass S sets every probability of the row
+  auto kadd = [](float& sum, float& comp, float t) {
+    const float y = t - comp;
+    const float z = sum + y;
+    comp = (z - sum) - y;
+    sum = z;
+  };
   long long cnt = 0;
-  float mass = 0.f;
+  float mass = 0.f, mass_c = 0.f;
   for (int d = d0; d < d1; d += 4) {  // four bins at a time (the loads and exps overlap)
     uint32_t c[4];
     float e[4];
@@ -492,8 +516,9 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (c[u] != 0u) { cnt += c[u]; mass += (float)c[u] * e[u]; }
+      if (c[u] != 0u) { cnt += c[u]; kadd(mass, mass_c, (float)c[u] * e[u]); }
   }
+  mass -= mass_c;
   // exclusive prefixes over the lanes (bins before the lane's first)
   long long ci = cnt;
   float mi = mass;
@@ -517,14 +542,14 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
     float my_s = 0.f;
     if (l == src) {
       long long cc = cpre;
-      float mm = mpre;
+      float mm = mpre, mm_c = 0.f;
       for (int d = d0; d < d1; ++d) {
         const uint32_t c = hist[d];
         if (c == 0u) continue;
         const float e = e_of(d);
-        if (cc + c >= k) { my_dk = d; my_tk = (int)(k - cc); my_s = mm + (float)my_tk * e; break; }
+        if (cc + c >= k) { my_dk = d; my_tk = (int)(k - cc); kadd(mm, mm_c, (float)my_tk * e); my_s = mm - mm_c; break; }
         cc += c;
-        mm += (float)c * e;
+        kadd(mm, mm_c, (float)c * e);
       }
     }
     dk = __shfl_sync(0xFFFFFFFFu, my_dk, src);
@@ -537,7 +562,7 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
     int cd = -1, cn = 0;
     float cb = 0.f;
     long long ccb = 0;
-    float cum = mpre;
+    float cum = mpre, cum_c = 0.f;  // cum - cum_c: the compensated running mass
     long long cc = cpre;
     const int dend = min(d1, dk + 1);
     for (int d = d0; d < dend && cd < 0; d += 4) {  // four bins at a time, then in order
@@ -555,15 +580,18 @@ __device__ bool warp_select(const RowCtx& x, float lmax, float s_all, const uint
         const float e = e4[u];
         const long long avail = (x.topk && d + u == dk) ? tk : (long long)c;
         const float md = (float)avail * e;
-        const float nxt = cum + md;
-        if (md > 0.f && nxt >= target) {
-          long long n = (long long)ceilf(__fdiv_rn(target - cum, e));
+        float nxt = cum, nxt_c = cum_c;
+        kadd(nxt, nxt_c, md);
+        if (md > 0.f && nxt - nxt_c >= target) {
+          const float base = cum - cum_c;
+          long long n = (long long)ceilf(__fdiv_rn(target - base, e));
           if (n < 1) n = 1;
           if (n > avail) n = avail;
-          cd = d + u; cn = (int)n; cb = cum; ccb = cc;
+          cd = d + u; cn = (int)n; cb = base; ccb = cc;
           continue;
         }
         cum = nxt;
+        cum_c = nxt_c;
         cc += c;
       }
     }
@@ -679,12 +707,17 @@ __device__ void generic_thresholds(const Group& g, RowShared& sh, const T* row, 
   }
   auto in_k1 = [&](uint32_t key, long long id) { return key > kk1 || (key == kk1 && id <= id1); };
   auto mass_ge = [&](uint32_t kk) -> float {
-    float m = 0.f;
+    float m = 0.f, mc = 0.f;  // compensated per-thread sum
     visit_row<T>(row, L, V, [&](uint32_t bits, long long id) {
       const uint32_t key = order_key(bits);
-      if (key >= kk && in_k1(key, id)) m += ex2((__uint_as_float(bits) - lmax) * x.c);
+      if (key >= kk && in_k1(key, id)) {
+        const float y = ex2((__uint_as_float(bits) - lmax) * x.c) - mc;
+        const float z = m + y;
+        mc = (z - m) - y;
+        m = z;
+      }
     });
-    return group_sum(g, m, sh.fscr);
+    return group_sum(g, m - mc, sh.fscr);
   };
   uint32_t kcut = kk1;
   long long idcut = id1, keptc = k1count;
@@ -769,7 +802,7 @@ __device__ bool finish_row(const RowArgs& A, RowShared& sh, const RowCtx& x, con
   }
   // warp merge (fixed butterfly), then the warps in order
   const float wfm = warp_reduce(acc.fm, [](float a, float b) { return fmax_nan(a, b); });
-  const float mine = (acc.s == 0.f || acc.fm == -INFINITY) ? 0.f : acc.s * ex2((acc.fm - wfm) * x.c);
+  const float mine = (acc.s == 0.f || acc.fm == -INFINITY) ? 0.f : (acc.s - acc.sc) * ex2((acc.fm - wfm) * x.c);
   const float ws = x.need_sum ? warp_reduce(mine, [](float a, float b) { return a + b; }) : 0.f;
   const long long wam = warp_min_i64(acc.fm == wfm ? acc.amax : LLONG_MAX);
   if (l == 0) { sh.w_fm[w] = wfm; sh.w_s[w] = ws; sh.w_amax[w] = wam; }

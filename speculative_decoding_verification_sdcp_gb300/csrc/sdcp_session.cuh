@@ -71,7 +71,6 @@ struct SessSmem {
   double cta_sum;      // the slice's total weight (read by the cluster)
   long long cta_cnt;   // the slice's tie count (read by the cluster)
   double owner_base;
-  double dscr[2 * 32 + 4];
   long long owner_pre, owner_carry;
   long long result;    // a tie id found by this CTA (read by the cluster)
   int st, a, draw;
@@ -124,10 +123,11 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
   const int64_t R_T = A.total + A.B;
   const int64_t V = A.V;
   const bool rule2 = (P.rule_id == 2u);
+  const bool relaxed = (P.rule_id == SDCP_RULE_RELAXED_TOP_K);
   const uint32_t tm = P.temperature_milli;
   const float c = (tm == 0u) ? 0.f : profile_c(tm);
   int st = SDCP_S_OK;
-  if ((P.rule_id != 1u && P.rule_id != 2u) || P.top_p_milli > 1000u) st = SDCP_S_BAD_PARAMS;
+  if ((P.rule_id != 1u && P.rule_id != 2u && !relaxed) || P.top_p_milli > 1000u) st = SDCP_S_BAD_PARAMS;
   else if (!offsets_ok) st = SDCP_S_BAD_PARAMS;
   else if (M < 1 || M > SDCP_MAX_M) st = SDCP_S_LIMIT;
   else if (rule2 && A.draft == nullptr) st = SDCP_S_Q_UNAVAILABLE;
@@ -161,6 +161,8 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
             const double u = session_uniform(A, b, P, (uint32_t)i, 0u);
             rej[h] = !(u < (double)ratio);
           }
+        } else if (relaxed) {  // x must lie in p's kept set (a finite logit)
+          rej[h] = !(sp.flags & SDCP_ROW_X_KEPT);
         } else {
           rej[h] = (x != sp.argmax);
         }
@@ -179,7 +181,7 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
     if (a > M) a = (int)M;
   }
   const bool ok = (st == SDCP_S_OK);
-  const bool draw = ok && rule2 && tm != 0u;
+  const bool draw = ok && (rule2 || relaxed) && tm != 0u;
   if (write && lane == 0) {
     A.status[b] = st;
     A.accepted[b] = ok ? a : 0;
@@ -211,18 +213,23 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
 // The draw.
 // ---------------------------------------------------------------------------------
 
-// Weight of token j: p_j = 2^(l_j c - bias) over the kept set, where c = log2(e) 1000/T and
-// bias = lmax c + log2(S); kept = value above the cut value, or the cut value and id <= tie
-// (values compare as floats: -0 and +0 are one value, as their order keys are).
+// Weight of token j: p_j = 2^((l_j - lmax) c) / S over the kept set, where c = log2(e) 1000/T
+// (l_j - lmax is exact near the maximum, where the mass is, so the weights carry no shared
+// rounding of a large exponent offset; 1/S is one correctly rounded division); kept = value
+// above the cut value, or the cut value and id <= tie (values compare as floats: -0 and +0
+// are one value, as their order keys are).
 struct DrawRow {
-  float c, bias;
+  float c, lmax, inv_s;
   float thr;  // the cut value (-inf: no cut)
   int tie;    // INT_MAX: every token of the cut value is kept
 };
+__device__ __forceinline__ float row_weight(const DrawRow& r, float v) {
+  return ex2((v - r.lmax) * r.c) * r.inv_s;
+}
 template <bool FILT>
 __device__ __forceinline__ float draw_weight(const DrawRow& r, uint32_t bits, int j) {
   const float v = __uint_as_float(bits);
-  const float e = ex2(fmaf(v, r.c, -r.bias));
+  const float e = row_weight(r, v);
   if (!FILT) return e;
   return (v > r.thr || (v == r.thr && j <= r.tie)) ? e : 0.f;
 }
@@ -366,7 +373,7 @@ __device__ void draw_pass(const SegSlice& sl, SessSmem& sm, const T* prow, const
 template <typename T, bool FILT>
 __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p, bool al_q, int V,
                          const DrawRow& pr, const DrawRow& qr, int k0, int k1, double carry,
-                         double target, bool last_only) {
+                         double target) {
   const int lane = threadIdx.x & 31;
   int lastpos = -1;
   for (int k = k0; k < k1; ++k) {
@@ -380,16 +387,19 @@ __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p,
 #pragma unroll
     for (int e = 0; e < kEpt; ++e) if (wv[e] > 0.f) lp = j0 + e;
     lastpos = max(lastpos, __reduce_max_sync(0xFFFFFFFFu, lp));
-    if (last_only) continue;
     float incl = ls;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float tv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
       if (lane >= o) incl += tv;
     }
-    const double start = carry + (double)(incl - ls);
+    // the lanes' intervals tile the segment: lane l covers [carry + incl(l-1), carry +
+    // incl(l)), so a target never falls between two lanes, whatever the rounding of incl
+    float ex = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+    if (lane == 0) ex = 0.f;
+    const double start = carry + (double)ex;
     int hit = INT_MAX;
-    if (start <= target && target < start + (double)ls) {
+    if (ls > 0.f && start <= target && target < carry + (double)incl) {
       double cc = start;
 #pragma unroll
       for (int e = 0; e < kEpt; ++e) {
@@ -412,8 +422,9 @@ __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p,
 // ---------------------------------------------------------------------------------
 
 // Returns W (the same in every CTA), or NaN when some CTA of the cluster flagged its pass
-// as unusable (sm.overflow).  Tie ids come from the CTAs' candidates when `ties`.  Segment
-// sums are fp32; every sum across segments, slices and CTAs is fp64.
+// as unusable (sm.overflow).  Tie ids come from the CTAs' candidates when `ties`.  Sums
+// within a CTA's slice are fp32 (a scan of at most 2048 segment sums: about 20 roundings);
+// the slices' totals, the target u * W and the owner's base are fp64.
 template <typename T, bool FILT>
 __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                               const SegSlice& sl, const T* prow, const T* qrow, bool residual,
@@ -422,14 +433,14 @@ __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, Se
   const int t = threadIdx.x, w = t >> 5, lane = t & 31;
   const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
   const int gpt = (sl.ngrp + g.nthreads - 1) / g.nthreads;
-  double loc = 0.0;
+  float loc = 0.f;
   for (int i = 0; i < gpt; ++i) {
     const int k = t * gpt + i;
-    if (k < sl.ngrp) loc += (double)sm.seg[k];
+    if (k < sl.ngrp) loc += sm.seg[k];
   }
-  double Wc;
-  const double pre = group_excl_scan_d(g, loc, sm.dscr, &Wc);
-  if (t == 0) { sm.cta_sum = Wc; sm.cta_ovf = sm.overflow; }
+  float Wc;
+  const float pre = group_excl_scan(g, loc, sm.fscr, &Wc);
+  if (t == 0) { sm.cta_sum = (double)Wc; sm.cta_ovf = sm.overflow; }
   cluster.sync();
   double W = 0.0;
   int owner = -1, lastr = -1, tp_id = INT_MAX, tq_id = INT_MAX, bad = 0;
@@ -444,49 +455,44 @@ __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, Se
   }
   const double target = u1 * W;
   {
+    // the owner is the last slice with weight whose start is at or below the target (the
+    // slices tile [0, W) by construction, whatever the rounding of their sums)
     double acc = 0.0;
     for (unsigned r = 0; r < C; ++r) {
       const double sr = *cluster.map_shared_rank(&sm.cta_sum, r);
-      if (owner < 0 && sr > 0.0 && acc <= target && target < acc + sr) { owner = (int)r; obase = acc; }
+      if (sr > 0.0 && acc <= target) { owner = (int)r; obase = acc; }
       acc += sr;
     }
   }
   cluster.sync();  // every CTA has read the slice totals
   if (bad) return kNaN64;
   if (!(W > 0.0)) return W;
-  const bool mine = (owner == (int)rank) || (owner < 0 && lastr == (int)rank);
-  if (!mine) return W;
+  (void)lastr;
+  if (owner != (int)rank) return W;
   pr.tie = pp ? tp_id : INT_MAX;
   qr.tie = qp ? tq_id : INT_MAX;
-  long long cand = LLONG_MAX, lastg = -1;
-  double cbase = 0.0;
-  if (owner >= 0) {
-    double bsum = obase + pre;
+  // the group: the last one with weight whose start is at or below the target (groups tile
+  // the slice by construction; a target past the slice's rounded end takes its last group,
+  // whose walk then ends on its last token with weight)
+  long long cand = -1;
+  float cbase = 0.f;
+  {
+    const float tloc = (float)(target - obase);  // the target within this slice
+    float bsum = pre;
     for (int i = 0; i < gpt; ++i) {
       const int k = t * gpt + i;
       if (k >= sl.ngrp) break;
-      const double sk = (double)sm.seg[k];
-      if (cand == LLONG_MAX && sk > 0.0 && bsum <= target && target < bsum + sk) { cand = k; cbase = bsum; }
+      const float sk = sm.seg[k];
+      if (sk > 0.f && bsum <= tloc) { cand = k; cbase = bsum; }
       bsum += sk;
     }
   }
-  for (int i = 0; i < gpt; ++i) {
-    const int k = t * gpt + i;
-    if (k < sl.ngrp && sm.seg[k] > 0.f) lastg = k;
-  }
-  const long long og = group_min_i64(g, cand, sm.lscr);
-  if (og != LLONG_MAX && cand == og) sm.owner_base = cbase;
-  const long long lg = group_max_i64(g, lastg, sm.lscr);
+  const long long og = group_max_i64(g, cand, sm.lscr);
+  if (og >= 0 && cand == og) sm.owner_base = obase + (double)cbase;
   g.sync();
-  if (w == 0) {
-    int tok;
-    if (og != LLONG_MAX) {
-      tok = draw_walk<T, FILT>(prow, qrow, residual, al_p, al_q, V, pr, qr, sl.grp_lo((int)og),
-                               sl.grp_hi((int)og), sm.owner_base, target, false);
-    } else {  // u * W rounded up to the end: the largest id with positive weight
-      tok = draw_walk<T, FILT>(prow, qrow, residual, al_p, al_q, V, pr, qr, sl.grp_lo((int)lg),
-                               sl.grp_hi((int)lg), 0.0, 0.0, true);
-    }
+  if (w == 0 && og >= 0) {
+    const int tok = draw_walk<T, FILT>(prow, qrow, residual, al_p, al_q, V, pr, qr, sl.grp_lo((int)og),
+                                       sl.grp_hi((int)og), sm.owner_base, target);
     if (lane == 0) *out = tok;
   }
   return W;
@@ -533,8 +539,8 @@ __device__ void tie_append(SessSmem& sm, const Raw8<T>& rp, const Raw8<T>& rq, b
   for_each8<T>(rp, rq, [&](uint32_t xp, uint32_t xq, int e) {
     if ((amb >> e) & 1u) {
       const float vp = __uint_as_float(xp), vq = __uint_as_float(xq);
-      const float P = (vp >= pr.thr) ? ex2(fmaf(vp, pr.c, -pr.bias)) : 0.f;
-      const float Q = (residual && vq >= qr.thr) ? ex2(fmaf(vq, qr.c, -qr.bias)) : 0.f;
+      const float P = (vp >= pr.thr) ? row_weight(pr, vp) : 0.f;
+      const float Q = (residual && vq >= qr.thr) ? row_weight(qr, vq) : 0.f;
       const int ep = (cp >> e) & 1u, eq = (cq >> e) & 1u;
       sm.ties[w][pos] = TieEntry{j0 + e, P, Q, ep | (eq << 1) | (st << 8), lp, lq};
       ++pos;
@@ -653,8 +659,8 @@ __device__ double draw_token_ties(cg::cluster_group& cluster, const Group& g, Se
         for_each8<T>(rp[u], rq[u], [&](uint32_t bp, uint32_t bq, int e) {
           const float vp = __uint_as_float(bp), vq = __uint_as_float(bq);
           const bool tp = pp && vp == pr.thr, tq = qp && vq == qr.thr;
-          float x = (vp >= pr.thr) ? ex2(fmaf(vp, pr.c, -pr.bias)) : 0.f;
-          if (residual) x = fmaxf(x - ((vq >= qr.thr) ? ex2(fmaf(vq, qr.c, -qr.bias)) : 0.f), 0.f);
+          float x = (vp >= pr.thr) ? row_weight(pr, vp) : 0.f;
+          if (residual) x = fmaxf(x - ((vq >= qr.thr) ? row_weight(qr, vq) : 0.f), 0.f);
           const bool am = tp || tq;  // on a cut value: weighed after the pass
           amb |= (am ? 1u : 0u) << e;
           cp |= (tp ? 1u : 0u) << e;
@@ -786,8 +792,8 @@ __device__ double draw_stream(cg::cluster_group& cluster, const Group& g, SessSm
         } else {
           const float vp = __uint_as_float(bp), vq = __uint_as_float(bqq);
           const bool tp = pp && vp == pr.thr, tq = qp && vq == qr.thr;
-          float x = (vp >= pr.thr) ? ex2(fmaf(vp, pr.c, -pr.bias)) : 0.f;
-          if (residual) x = fmaxf(x - ((vq >= qr.thr) ? ex2(fmaf(vq, qr.c, -qr.bias)) : 0.f), 0.f);
+          float x = (vp >= pr.thr) ? row_weight(pr, vp) : 0.f;
+          if (residual) x = fmaxf(x - ((vq >= qr.thr) ? row_weight(qr, vq) : 0.f), 0.f);
           const bool am = tp || tq;
           amb |= (am ? 1u : 0u) << e;
           cp |= (tp ? 1u : 0u) << e;
@@ -1089,11 +1095,11 @@ __device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem
         j = K.id[w][i];
         const float v = K.v[w][i];
         const bool kp = v > pr.thr || (v == pr.thr && j <= pr.tie);
-        x = kp ? ex2(fmaf(v, pr.c, -pr.bias)) : 0.f;
+        x = kp ? row_weight(pr, v) : 0.f;
         if (residual && x > 0.f) {
           const float vq = K.r[w][i];
           const bool kq = vq > qr.thr || (vq == qr.thr && j <= qr.tie);
-          if (kq) x = fmaxf(x - ex2(fmaf(vq, qr.c, -qr.bias)), 0.f);
+          if (kq) x = fmaxf(x - row_weight(qr, vq), 0.f);
         }
       }
       float incl = x;
@@ -1169,19 +1175,24 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
   const int64_t R_T = A.total + A.B;
   const int V = (int)A.V;
   const T* trow = reinterpret_cast<const T*>(A.target) + (off0 + b + a) * (int64_t)V;
-  const T* drow = reinterpret_cast<const T*>(A.draft) + (off0 + (a < M ? a : 0)) * (int64_t)V;
+  // the residual max(0, p_a - q_a) at Rule 2's first rejection; else a draw from p_a alone
+  // (Rule 2's bonus, and every draw of the relaxed rule)
+  bool residual = (a < M) && P.rule_id == 2u;
+  const T* drow = residual ? reinterpret_cast<const T*>(A.draft) + (off0 + a) * (int64_t)V
+                           : reinterpret_cast<const T*>(A.target) + (off0 + b + a) * (int64_t)V;
   const RowStat sp = load_stat(A.stats + off0 + b + a);
-  const RowStat sq = (a < M) ? load_stat(A.stats + R_T + off0 + a) : sp;
+  const RowStat sq = residual ? load_stat(A.stats + R_T + off0 + a) : sp;
   const float c = profile_c(P.temperature_milli);
   const bool al_p = ((uintptr_t)trow & 15u) == 0, al_q = ((uintptr_t)drow & 15u) == 0;
   const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
-  bool residual = (a < M);
   const bool filt_p = sp.thr_key != 0u || sp.thr_n != INT_MAX;
   const bool filt_q = residual && (sq.thr_key != 0u || sq.thr_n != INT_MAX);
   DrawRow pr, qr;
   pr.c = qr.c = c;
-  pr.bias = fmaf(sp.lmax, c, log2f(sp.s));
-  qr.bias = fmaf(sq.lmax, c, log2f(sq.s));
+  pr.lmax = sp.lmax;
+  qr.lmax = sq.lmax;
+  pr.inv_s = __fdiv_rn(1.f, sp.s);
+  qr.inv_s = __fdiv_rn(1.f, sq.s);
   pr.thr = filt_p ? key_value(sp.thr_key) : -INFINITY;
   qr.thr = filt_q ? key_value(sq.thr_key) : -INFINITY;
   pr.tie = INT_MAX;

@@ -39,7 +39,8 @@ class Workload:
     sigma: float = 2.0             # std of the target logits
     noise: float = 0.5             # std of the drafter's disagreement
     draft_scale: float = 1.0       # drafter logits = draft_scale * target + noise
-    rules: str = "spec"            # "greedy", "spec", or "alternate" (even greedy, odd spec)
+    rules: str = "spec"            # "greedy", "spec", "relaxed" (private rule 192), or
+                                   # "alternate" (even greedy, odd spec)
     temperature_milli: int | tuple = 1000   # constant, or a tuple drawn from per session
     top_k: int = 0
     top_p_milli: int = 1000
@@ -137,6 +138,8 @@ def make_params(w: Workload, gen: np.random.Generator) -> np.ndarray:
         p["rule_id"] = 1
     elif w.rules == "spec":
         p["rule_id"] = 2
+    elif w.rules == "relaxed":
+        p["rule_id"] = 192
     else:
         p["rule_id"] = np.where(b % 2 == 0, 1, 2)
     if isinstance(w.temperature_milli, tuple):

@@ -5,8 +5,9 @@ where a decision lies within 1e-5 (relative) of its boundary in the oracle's own
 arithmetic, and then the GPU's outcome must be the one on the other side of that boundary:
   * acceptance: the uniform within 1e-5 of min(1, p/q) at the first position where the
     two accepted counts part;
-  * draw: u * W within 1e-5 * W of the edge shared by the oracle's token and the GPU's
-    token, which must be neighbours among the tokens of positive weight (ids ascending);
+  * draw: the GPU's token has positive weight and u * W lies within 1e-5 * W of its
+    cumulative interval (ids ascending), so the tokens between it and the oracle's token
+    weigh less than 1e-5 * W in all;
   * top-p crossing (SDCP Section 4.1): where a row's cumulative mass lies within 1e-5 of
     P, any crossing between the oracle's crossings for P (1 - 1e-5) and P (1 + 1e-5) is a
     faithful reading; the GPU's crossing must lie in that band, and the session must then
@@ -88,25 +89,21 @@ def _draw_cdf(T, D, off, b, a, prm, mode, force=None):
 
 
 def _check_draw_boundary(C, W, u1, tg, to, b):
-    """The GPU's token tg and the oracle's token to must be neighbours among the tokens of
-    positive weight, and u * W must lie within BOUNDARY * W of the edge they share."""
+    """A draw that differs is a boundary case when u * W lies within BOUNDARY * W of the
+    GPU token's own cumulative interval (ids ascending) and that token has positive weight:
+    every token between the two then carries less than BOUNDARY * W in all."""
     V = C.shape[0]
     assert 0 <= tg < V, "session %d: GPU token %d out of range" % (b, tg)
     lo_g = C[tg - 1] if tg > 0 else 0.0
     hi_g = C[tg]
     assert hi_g > lo_g, "session %d: GPU drew token %d of zero weight" % (b, tg)
-    lo_o = C[to - 1] if to > 0 else 0.0
-    hi_o = C[to]
-    if tg < to:
-        edge = hi_g
-        assert lo_o == hi_g, "session %d: tokens %d (GPU) and %d (oracle) are not neighbours" % (b, tg, to)
-    else:
-        edge = lo_g
-        assert hi_o == lo_g, "session %d: tokens %d (GPU) and %d (oracle) are not neighbours" % (b, tg, to)
     target = u1 * W
-    assert abs(target - edge) <= BOUNDARY * W, (
-        "session %d: GPU token %d, oracle token %d: u*W=%r is %r from their shared edge (W=%r)" % (
-            b, tg, to, target, abs(target - edge), W))
+    lo_o = C[to - 1] if to > 0 else 0.0
+    assert lo_o <= target < C[to] or target >= W, (b, to, target)  # the oracle's own token
+    gap = 0.0 if lo_g <= target < hi_g else min(abs(target - lo_g), abs(target - hi_g))
+    assert gap <= BOUNDARY * W, (
+        "session %d: GPU token %d, oracle token %d: u*W=%r is %r from the GPU token's interval "
+        "[%r, %r) (W=%r)" % (b, tg, to, target, gap, lo_g, hi_g, W))
 
 
 def topp_band(logits, tm, k, p):
@@ -150,6 +147,47 @@ def _forced_session(T, D, off, x, params, b, gs, session_ids=None):
     return args, force, oracle.verify_batch(*args, force_kept=force, session_ids=_sid(session_ids, b))
 
 
+def _draw_diagnostics(T, D, off, params, b, a, mode, gs, det, force):
+    """What the GPU and the oracle each made of the draw's rows (for a failure message)."""
+    B = params.shape[0]
+    R_T = int(off[-1]) + B
+    prm = params[b]
+    tm, k, p = int(prm["temperature_milli"]), int(prm["top_k"]), int(prm["top_p_milli"])
+    rows = [("p", int(off[b]) + b + a, T[int(off[b]) + b + a])]
+    if mode == oracle.EXTRA_RESIDUAL:
+        rows.append(("q", R_T + int(off[b]) + a, D[int(off[b]) + a]))
+    lines = ["draw of session %d at position %d (mode %d), u1=%r" % (b, a, mode, float(det["u1"][b]))]
+    for name, r, logits in rows:
+        info = oracle.row_dist(logits, tm, k, p, want_dist=False)[2]
+        band = topp_band(logits, tm, k, p) if info.topp_target >= 0 else None
+        g = "n/a" if gs is None else "kept=%d log_s=%.9g thr_n=%d flags=%d" % (
+            int(gs[r]["kept"]), float(gs[r]["log_s"]), int(gs[r]["thr_n"]), int(gs[r]["flags"]))
+        lines.append("  %s row %d: oracle kept=%d log_s=%.9g margin=%.3g band=%s | gpu %s" % (
+            name, r, info.kept, info.log_s, _row_margin(info), band, g))
+    if gs is not None:
+        u1 = float(det["u1"][b])
+        fp = int(gs[rows[0][1]]["kept"])
+        fq = int(gs[rows[1][1]]["kept"]) if len(rows) > 1 else -1
+        pa, kp = oracle.row_dist(rows[0][2], tm, k, p, want_kept=True, force_kept=fp)[:2]
+        qa, kq = oracle.row_dist(rows[1][2], tm, k, p, want_kept=True, force_kept=fq)[:2] if len(rows) > 1 else (None, None)
+        C2, W2 = oracle.draw_cdf(pa, qa)
+        tok = int(np.searchsorted(C2, u1 * W2, side="right"))
+        lines.append("  oracle draw with the GPU's kept counts: token %d (W=%r)" % (tok, W2))
+
+        # and with the GPU's normalisers too: p_j = exp((l_j - lmax)/T) / S_gpu on the kept set
+        def with_gpu_s(logits, kept, r):
+            l = logits.astype(np.float64) if logits.dtype == np.float32 else \
+                (logits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            z = (l - l.max()) / (tm / 1000.0)
+            return np.where(kept.astype(bool), np.exp(z - float(gs[r]["log_s"])), 0.0)
+        pg = with_gpu_s(rows[0][2], kp, rows[0][1])
+        qg = with_gpu_s(rows[1][2], kq, rows[1][1]) if len(rows) > 1 else None
+        C3, W3 = oracle.draw_cdf(pg, qg)
+        tok3 = int(np.searchsorted(C3, u1 * W3, side="right"))
+        lines.append("  oracle draw with the GPU's kept counts and log S: token %d (W=%r)" % (tok3, W3))
+    return "\n".join(lines)
+
+
 def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None, force=None,
                      session_ids=None):
     """One session; adds to counts; raises AssertionError on a real disagreement.  force:
@@ -164,7 +202,7 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
         counts["exact"] += 1
         return
     rule = int(params["rule_id"][b])
-    assert rule == 2, "greedy session %d differs: gpu a=%d tokens=%s, oracle a=%d tokens=%s" % (
+    assert rule in (2, 192), "greedy session %d differs: gpu a=%d tokens=%s, oracle a=%d tokens=%s" % (
         b, got["accepted"][b], got["out_tokens"][slot], ref["accepted"][b], ref["out_tokens"][slot])
     if topp_ok and det["topp_margin"][b] <= BOUNDARY:
         # a top-p crossing within rounding of P: the session must match the oracle run with
@@ -174,8 +212,14 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
         if gs is not None:
             args, force2, r2 = _forced_session(T, D, off, x, params, b, gs, session_ids)
             c2 = {"exact": 0, "accept_boundary": 0, "draw_boundary": 0, "topp_boundary": 0}
-            _compare_session(mine, r2, *args, 0, c2, topp_ok=False, force=force2,
-                             session_ids=_sid(session_ids, b))
+            try:
+                _compare_session(mine, r2, *args, 0, c2, topp_ok=False, force=force2,
+                                 session_ids=_sid(session_ids, b))
+            except AssertionError as e:
+                a = int(got["accepted"][b])
+                mode = int(r2["detail"]["extra_mode"][0])
+                raise AssertionError("%s\n(full batch) %s" % (
+                    e, _draw_diagnostics(T, D, off, params, b, a, mode, gs, det, None)))
             counts["topp_boundary"] += 1
             return
         args = session_arrays(T, D, off, x, params, b)
@@ -208,10 +252,14 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
     rt = ref["out_tokens"][o0 + b:o0 + b + a + 1]
     assert np.array_equal(gt[:a], rt[:a]) and got["n_out"][b] == a + 1
     mode = int(det["extra_mode"][b])
-    assert mode in (oracle.EXTRA_RESIDUAL, oracle.EXTRA_BONUS, oracle.EXTRA_RESIDUAL_AS_P), mode
+    assert mode in (oracle.EXTRA_RESIDUAL, oracle.EXTRA_BONUS, oracle.EXTRA_RESIDUAL_AS_P,
+                    oracle.EXTRA_FROM_P), mode
     m2 = oracle.EXTRA_RESIDUAL if mode == oracle.EXTRA_RESIDUAL else oracle.EXTRA_BONUS
     C, W = _draw_cdf(T, D, off, b, a, params[b], m2, force)
-    _check_draw_boundary(C, W, float(det["u1"][b]), int(gt[a]), int(rt[a]), b)
+    try:
+        _check_draw_boundary(C, W, float(det["u1"][b]), int(gt[a]), int(rt[a]), b)
+    except AssertionError as e:
+        raise AssertionError(str(e) + "\n" + _draw_diagnostics(T, D, off, params, b, a, m2, gs, det, force))
     counts["draw_boundary"] += 1
     # only the drawn slot may differ
     assert np.array_equal(got["out_tokens"][o0 + b + a + 1:o1 + b + 1],

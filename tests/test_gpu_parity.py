@@ -239,3 +239,53 @@ def test_full_size_workloads(name):
     got, counts = _parity(batch, name=name)
     assert (got["status"] == 0).all(), np.unique(got["status"], return_counts=True)
     assert counts["rows"]["fallback"] == 0, counts
+
+
+@pytest.mark.parametrize("name", ["topk50", "large_batch_mixed"])
+def test_two_phase_path(name):
+    """sdcp_verify_rows then sdcp_verify_sessions (the separate completion kernel, thread-block
+    clusters and streamed draws) against the oracle, like the one-call path above."""
+    import oracle
+    import parity
+    from speculative_decoding_verification_sdcp_gb300.sdcp import Verifier
+    batch = synth.make_batch(synth.WORKLOADS[name], device=DEV)
+    ver = Verifier(batch.V, batch.B, batch.total_drafts, DEV)
+    out = ver.phases(batch.target, batch.draft, batch.m_offsets, batch.draft_tokens, batch.params_dev)
+    torch.cuda.synchronize()
+    got = {k: t.cpu().numpy() for k, t in zip(("accepted", "n_out", "out_tokens", "status"), out)}
+    T, D, off, x = parity.host_arrays(batch)
+    ref = oracle.verify_batch(T, D, off, x, batch.params, nthreads=parity.ORACLE_THREADS)
+    gs = parity.gpu_row_stats(batch)
+    counts = parity.compare_verdicts(got, ref, T, D, off, x, batch.params, gs=gs)
+    parity.check_invariants(got, off, x, batch.params, batch.V)
+    parity.report("two_phase_" + name, counts)
+    assert counts["exact"] >= batch.B - 2, counts
+
+
+RELAXED = [
+    # dtype, V, M, T, top_k, top_p
+    (synth.BF16, 32000, 6, 700, 50, 1000),
+    (synth.F32, 4099, ("uniform", 1, 9), 1000, 3, 900),
+    (synth.BF16, 50257, 4, 0, 0, 1000),        # temperature 0: the greedy rule
+    (synth.BF16, 32000, 5, 800, 0, 900),       # the kept set of a top-p cut
+    (synth.BF16, 65536, 3, 900, 1, 1000),      # top-1: the greedy rule again
+]
+
+
+@pytest.mark.parametrize("case", RELAXED, ids=lambda c: "dt%d-V%d-T%d-k%d-p%d" % (c[0], c[1], c[3], c[4], c[5]))
+def test_relaxed_rule(case):
+    """The private-use relaxed rule (id 192): accept while x is in p's kept set, then a draw
+    from p; it reads no draft rows, so the call also runs without draft logits."""
+    import oracle
+    import parity
+    dt, V, m, T, k, p = case
+    w = synth.custom_workload(B=16, V=V, dtype=dt, m=m, rules="relaxed", temperature_milli=T, top_k=k,
+                              top_p_milli=p, sigma=3.0, noise=1.0, seed_base=321,
+                              gen_seed=500 + RELAXED.index(case))
+    batch = synth.make_batch(w, device=DEV)
+    got, counts = _parity(batch, name="relaxed_%d" % RELAXED.index(case))
+    assert (got["status"] == 0).all()
+    assert counts["exact"] >= batch.B - 2, counts
+    got2 = parity.run_gpu(batch, with_draft=False)
+    for key in got:
+        assert np.array_equal(got[key], got2[key]), key

@@ -552,3 +552,77 @@ def test_row_stats_batch_row_order_and_tokens(oracle_mod):
         if xi < V:
             assert lpx[r] == (np.log(dist[xi]) if kept[xi] else -np.inf)
         r += 1
+
+
+# ---------------------------------------------------------------------------------------
+# The relaxed rule (private use id 192): accept while x[i] is in p[i]'s kept set
+# ---------------------------------------------------------------------------------------
+def _relaxed_batch(oracle_mod, B=30, V=40, M=4, seed=12):
+    rng = np.random.default_rng(seed)
+    off = np.arange(B + 1, dtype=np.int32) * M
+    T = rng.normal(0, 2, size=(B * M + B, V)).astype(np.float32)
+    x = rng.integers(0, V, size=B * M).astype(np.int32)
+    # make some proposals good: the target's own argmax or a near-top token
+    top = np.argsort(-T, axis=1, kind="stable")
+    rows = np.arange(B * M) + np.repeat(np.arange(B), M)
+    pick = rng.integers(0, 3, size=B * M)
+    x = np.where(rng.random(B * M) < 0.7, top[rows, pick], x).astype(np.int32)
+    return T, off, x
+
+
+def test_relaxed_rule_at_temperature_zero_is_greedy(oracle_mod):
+    T, off, x = _relaxed_batch(oracle_mod)
+    B = off.shape[0] - 1
+    r = oracle_mod.verify_batch(T, None, off, x, _params(oracle_mod, B, rule=192, T=0, k=5))
+    g = oracle_mod.verify_batch(T, None, off, x, _params(oracle_mod, B, rule=1))
+    for k in ("status", "accepted", "n_out", "out_tokens"):
+        assert np.array_equal(r[k], g[k]), k
+
+
+def test_relaxed_rule_with_top1_is_greedy(oracle_mod):
+    T, off, x = _relaxed_batch(oracle_mod)
+    B = off.shape[0] - 1
+    r = oracle_mod.verify_batch(T, None, off, x, _params(oracle_mod, B, rule=192, T=800, k=1))
+    g = oracle_mod.verify_batch(T, None, off, x, _params(oracle_mod, B, rule=1))
+    for k in ("status", "accepted", "n_out", "out_tokens"):
+        assert np.array_equal(r[k], g[k]), k
+
+
+def test_relaxed_rule_without_filter_is_rule2_with_q_equal_p(oracle_mod):
+    """Every finite token is kept: all M are accepted and the additional token is the draw
+    from p[M] that Rule 2 makes when q = p (same uniform, same row)."""
+    T, off, x = _relaxed_batch(oracle_mod)
+    B = off.shape[0] - 1
+    r = oracle_mod.verify_batch(T, None, off, x, _params(oracle_mod, B, rule=192, T=900, seed=7))
+    Ms = np.diff(off)
+    assert np.array_equal(r["accepted"], Ms)
+    rows = np.arange(B * Ms[0]) + np.repeat(np.arange(B), Ms[0])
+    D = T[rows]  # q = p: draft logits equal to the target logits of the same positions
+    g = oracle_mod.verify_batch(T, D, off, x, _params(oracle_mod, B, rule=2, T=900, seed=7))
+    for k in ("status", "accepted", "n_out", "out_tokens"):
+        assert np.array_equal(r[k], g[k]), k
+
+
+@pytest.mark.parametrize("k", [2, 5, 13])
+def test_relaxed_rule_accepts_by_rank(oracle_mod, k):
+    """a = the number of leading positions whose token ranks among the k largest logits of
+    its target row (order: logit descending, id ascending), by counting ranks here."""
+    T, off, x = _relaxed_batch(oracle_mod, seed=20 + k)
+    B = off.shape[0] - 1
+    r = oracle_mod.verify_batch(T, None, off, x, _params(oracle_mod, B, rule=192, T=1000, k=k))
+    for b in range(B):
+        o0, M = int(off[b]), int(off[b + 1] - off[b])
+        a = 0
+        while a < M:
+            row = T[o0 + b + a]
+            xi = int(x[o0 + a])
+            rank = int((row > row[xi]).sum() + ((row == row[xi]) & (np.arange(row.shape[0]) < xi)).sum())
+            if rank >= k:
+                break
+            a += 1
+        assert int(r["accepted"][b]) == a, (b, int(r["accepted"][b]), a)
+        # the additional token is one of the target row's k kept tokens
+        extra = int(r["out_tokens"][o0 + b + a])
+        row = T[o0 + b + a]
+        rank = int((row > row[extra]).sum() + ((row == row[extra]) & (np.arange(row.shape[0]) < extra)).sum())
+        assert rank < k

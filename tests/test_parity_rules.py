@@ -1,9 +1,10 @@
 """The comparison rules of the parity tests, checked on CPU with the oracle's own outputs
 (mistakes are planted in a copy of those outputs, never in a GPU run).
 
-A differing draw is accepted only where u * W lies within 1e-5 * W of the edge shared by
-the two tokens and the tokens are neighbours among the tokens of positive weight; a
-differing greedy session, or a draw far from any edge, must fail.
+A differing draw is accepted only where the GPU's token has positive weight and u * W lies
+within 1e-5 * W of that token's cumulative interval (so whatever lies between the two
+tokens weighs less than 1e-5 * W); a differing greedy session, or a draw far from u * W,
+must fail.
 """
 import numpy as np
 import pytest
@@ -16,19 +17,22 @@ def _cdf(weights):
     return C, float(C[-1])
 
 
-def test_draw_boundary_accepts_neighbours_at_their_edge():
+def test_draw_boundary_accepts_tokens_within_the_window():
     C, W = _cdf([0.2, 0.0, 0.3, 0.5])
     # edge between token 0 and token 2 (token 1 has no weight) is at 0.2
     u = 0.2 / W
     parity._check_draw_boundary(C, W, u + 3e-6, 0, 2, 0)
     parity._check_draw_boundary(C, W, u - 3e-6, 2, 0, 0)
+    # tokens of negligible weight between the two: still within the boundary window
+    C, W = _cdf([0.2, 1e-12, 2e-12, 0.3, 0.5])
+    parity._check_draw_boundary(C, W, (0.2 - 3e-6) / W, 3, 0, 0)
 
 
 @pytest.mark.parametrize("tg,to,u", [
     (0, 2, 0.25),     # far from the shared edge
-    (0, 3, 0.2),      # not neighbours: token 2 has weight between them
+    (3, 0, 0.19),     # token 2's weight lies between them
     (1, 2, 0.2),      # the GPU token has no weight
-    (3, 0, 0.2),      # not neighbours the other way
+    (3, 2, 0.3),      # u*W inside token 2, far from token 3
 ])
 def test_draw_boundary_rejects(tg, to, u):
     C, W = _cdf([0.2, 0.0, 0.3, 0.5])
