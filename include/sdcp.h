@@ -269,13 +269,22 @@ typedef struct sdcp_verify_options {
   const uint8_t* session_ids;   /* device, [B][16]: each session's 16-octet identifier
                                    (Section 5.2 session-id); needed by SDCP_RNG_HMAC_SHA256,
                                    ignored by Philox (which uses params[b].session_tag) */
+  const float* q_rows;          /* device, [total_drafts][V] binary32, or NULL: q given as the
+                                   drafter's rows of probabilities (Section 5.2 q_rows; q[i]
+                                   is row i of the session, Section 6.4 Rule 2), used as given
+                                   (no sampling profile).  Draft logits are then not read (they
+                                   may be NULL) and the first phase reads target rows only.
+                                   q(x) = 0 gives SDCP_S_BAD_PROPOSAL; a q(x) that is NaN,
+                                   infinite or negative gives SDCP_S_BAD_PARAMS; other values
+                                   of a row are used as given. */
 } sdcp_verify_options;
 
 /*
  * sdcp_verify_batch with options: the same arguments, layout and results, with the random
- * values chosen by opts->rng_id.  opts = NULL is sdcp_verify_batch.  Returns SDCP_E_INVALID
- * for an unknown rng_id, a struct_size below sizeof(sdcp_verify_options), or the HMAC
- * generator without session_ids.
+ * values chosen by opts->rng_id and q from the draft logits or from opts->q_rows.
+ * opts = NULL is sdcp_verify_batch.  Returns SDCP_E_INVALID for an unknown rng_id, a
+ * struct_size below sizeof(sdcp_verify_options), or the HMAC generator without session_ids;
+ * SDCP_E_ALIGN for q_rows not aligned to 4 bytes.
  */
 int sdcp_verify_batch_ex(const void* target_logits, const void* draft_logits, int dtype,
                          int64_t V, int32_t B, const int32_t* m_offsets, int64_t total_drafts,
@@ -380,7 +389,7 @@ int sdcp_split_sessions(const int32_t* m_offsets, const sdcp_session_params* par
 const char* sdcp_strerror(int code);
 
 /* ABI version of this header; bumps on any incompatible change. */
-#define SDCP_ABI_VERSION 1
+#define SDCP_ABI_VERSION 2
 int sdcp_abi_version(void);
 
 #ifdef __cplusplus

@@ -88,7 +88,7 @@ def lib():
         L.oracle_set_topp_shift.argtypes = [ctypes.c_double]
         L.oracle_set_topp_shift.restype = None
         L.oracle_verify_batch_rng.argtypes = [vp, vp, ctypes.c_int, i64, i32, vp, i64, vp, vp, vp,
-                                              vp, vp, vp, vp, vp, vp, ctypes.c_int]
+                                              vp, vp, vp, vp, vp, vp, vp, ctypes.c_int]
         L.oracle_row_dist_forced.argtypes = [vp, ctypes.c_int, i64, u32, u32, u32, vp, vp,
                                              ctypes.POINTER(RowInfo), i64]
         L.oracle_row_dist_forced.restype = ctypes.c_int
@@ -173,14 +173,16 @@ def draw(p: np.ndarray, q: np.ndarray | None, u: float) -> int:
 def verify_batch(target: np.ndarray, draft: np.ndarray | None, m_offsets: np.ndarray,
                  draft_tokens: np.ndarray, params: np.ndarray, nthreads: int = 1,
                  want_detail: bool = True, session_ids: np.ndarray | None = None,
-                 force_kept: np.ndarray | None = None):
+                 force_kept: np.ndarray | None = None, q_rows: np.ndarray | None = None):
     """Rules 1 and 2 of SDCP Section 6.4 over a ragged batch (layout of the C ABI).
 
     target: [total_drafts + B, V], draft: [total_drafts, V] or None (float32 or raw bf16
     bits as uint16).  session_ids ([B, 16] uint8) selects the draft's HMAC-SHA-256 random
     values (Section 6.4) instead of Philox.  force_kept ([2 total + B] int32, row order of
     the C ABI's row statistics, -1 = as defined) places top-p crossings (a parity-test
-    hook).  Returns a dict of numpy arrays (accepted, n_out, out_tokens, status, detail).
+    hook).  q_rows ([total, V] float32) gives q as rows of probabilities (SDCP Section 5.2)
+    instead of the draft logits.  Returns a dict of numpy arrays (accepted, n_out,
+    out_tokens, status, detail).
     """
     target = np.ascontiguousarray(target)
     dcode = _dtype_code(target)
@@ -206,9 +208,13 @@ def verify_batch(target: np.ndarray, draft: np.ndarray | None, m_offsets: np.nda
     if force_kept is not None:
         fk = np.ascontiguousarray(force_kept, dtype=np.int32)
         assert fk.shape == (2 * total + B,)
+    qr = None
+    if q_rows is not None:
+        qr = np.ascontiguousarray(q_rows, dtype=np.float32)
+        assert qr.shape == (total, V)
     rc = lib().oracle_verify_batch_rng(_ptr(target), _ptr(draft), dcode, V, B, _ptr(m_offsets),
                                        total, _ptr(draft_tokens), _ptr(params), _ptr(sid), _ptr(fk),
-                                       _ptr(acc), _ptr(nout), _ptr(toks), _ptr(st), _ptr(det),
+                                       _ptr(qr), _ptr(acc), _ptr(nout), _ptr(toks), _ptr(st), _ptr(det),
                                        int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify_batch rejected its arguments (rc=%d)" % rc)

@@ -412,7 +412,8 @@ static double topp_margin_of(const orc_row_info* in) {
 static void verify_session(const void* T, const void* D, int dtype, int64_t V,
                            const int32_t* m_offsets, int64_t total_drafts, int32_t b,
                            const int32_t* x, const orc_params* prm, const uint8_t* sid,
-                           const int32_t* force, int64_t R_T, int32_t* accepted, int32_t* n_out,
+                           const int32_t* force, int64_t R_T, const float* QR,
+                           int32_t* accepted, int32_t* n_out,
                            int32_t* out_tokens, int32_t* status, orc_detail* det) {
   size_t esz = (dtype == ORC_F32) ? 4 : 2;
   orc_detail dl;
@@ -430,7 +431,7 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
   else if (prm->top_p_milli > 1000) st = ORC_BAD_PARAMS;
   else if (!offsets_ok) st = ORC_BAD_PARAMS;
   else if (M < 1 || M > ORC_MMAX) st = ORC_LIMIT;
-  else if (prm->rule_id == 2 && D == NULL) st = ORC_Q_UNAVAILABLE;
+  else if (prm->rule_id == 2 && D == NULL && QR == NULL) st = ORC_Q_UNAVAILABLE;
   else {
     for (int64_t i = 0; i < M; ++i)
       if (x[off0 + i] < 0 || x[off0 + i] >= V) { st = ORC_BAD_PROPOSAL; break; }
@@ -465,7 +466,17 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
       double mg = topp_margin_of(&pin[i]);
       if (mg < det->topp_margin) det->topp_margin = mg;
     }
-    if (st == ORC_OK && rule2) {
+    if (st == ORC_OK && rule2 && QR) {
+      /* q given as rows of probabilities (Section 5.2 q_rows): used as given, no profile.
+         A value that is not a probability (NaN, infinite, negative) at x: no distribution;
+         q(x) = 0: the precondition fails (Section 6.3). */
+      for (int64_t i = 0; i < M && st == ORC_OK; ++i) {
+        double qx = (double)QR[(size_t)(off0 + i) * (size_t)V + (size_t)x[off0 + i]];
+        if (isnan(qx) || isinf(qx) || qx < 0.0) st = ORC_BAD_PARAMS;
+      }
+      for (int64_t i = 0; i < M && st == ORC_OK; ++i)
+        if (QR[(size_t)(off0 + i) * (size_t)V + (size_t)x[off0 + i]] == 0.0f) st = ORC_BAD_PROPOSAL;
+    } else if (st == ORC_OK && rule2) {
       qin = (orc_row_info*)calloc((size_t)M, sizeof(orc_row_info));
       qk = (uint8_t**)calloc((size_t)M, sizeof(uint8_t*));
       for (int64_t i = 0; i < M && st == ORC_OK; ++i) {
@@ -511,7 +522,12 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
     for (a = 0; a < M; ++a) {
       int32_t xi = x[off0 + a];
       double lp, lq;
-      if (tm == 0) { /* one-hot rows; q(x) = 1 by the precondition */
+      if (QR) { /* q(x) as given */
+        double lpx = logit_at(TROW(a), dtype, xi);
+        if (tm == 0) lp = (xi == pin[a].argmax) ? 0.0 : -INFINITY;
+        else lp = (pk[a][xi] && lpx != -INFINITY) ? lpx / t - pin[a].lmax / t - pin[a].log_s : -INFINITY;
+        lq = log((double)QR[(size_t)(off0 + a) * (size_t)V + (size_t)xi]);
+      } else if (tm == 0) { /* one-hot rows; q(x) = 1 by the precondition */
         lp = (xi == pin[a].argmax) ? 0.0 : -INFINITY;
         lq = 0.0;
       } else {
@@ -532,7 +548,11 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
     double* qa = (a < M) ? (double*)malloc(sizeof(double) * (size_t)V) : NULL;
     double* C = (double*)malloc(sizeof(double) * (size_t)V);
     row_dist_impl(TROW(a), dtype, V, tm, prm->top_k, prm->top_p_milli, pa, NULL, NULL, FT(a));
-    if (qa) row_dist_impl(DROW(a), dtype, V, tm, prm->top_k, prm->top_p_milli, qa, NULL, NULL, FD(a));
+    if (qa && QR) {
+      for (int64_t j = 0; j < V; ++j) qa[j] = (double)QR[(size_t)(off0 + a) * (size_t)V + (size_t)j];
+    } else if (qa) {
+      row_dist_impl(DROW(a), dtype, V, tm, prm->top_k, prm->top_p_milli, qa, NULL, NULL, FD(a));
+    }
     double u1 = verifier_uniform(prm, sid, (uint32_t)a, 1);
     det->u1 = u1;
     if (qa) {
@@ -586,13 +606,16 @@ static void verify_session(const void* T, const void* D, int dtype, int64_t V,
  */
 /* session_ids (optional, [B][16]) selects the HMAC derivation of the random values;
    force_kept (optional, [2 total + B], row order of the C ABI's row statistics) is the
-   parity tests' hook that places top-p crossings (-1: where the definition puts them). */
+   parity tests' hook that places top-p crossings (-1: where the definition puts them);
+   q_rows (optional, [total][V] binary32) gives q as rows of probabilities (Section 5.2
+   q_rows) instead of draft logits with the profile. */
 int oracle_verify_batch_rng(const void* T, const void* D, int dtype, int64_t V, int32_t B,
                             const int32_t* m_offsets, int64_t total_drafts,
                             const int32_t* draft_tokens, const orc_params* params,
                             const uint8_t* session_ids, const int32_t* force_kept,
-                            int32_t* accepted, int32_t* n_out, int32_t* out_tokens,
-                            int32_t* status, orc_detail* detail, int nthreads) {
+                            const float* q_rows, int32_t* accepted, int32_t* n_out,
+                            int32_t* out_tokens, int32_t* status, orc_detail* detail,
+                            int nthreads) {
   if (B < 0 || V < 1 || (dtype != ORC_F32 && dtype != ORC_BF16)) return 1;
   if (!T || !m_offsets || !draft_tokens || !params) return 1;
 #ifdef _OPENMP
@@ -602,7 +625,7 @@ int oracle_verify_batch_rng(const void* T, const void* D, int dtype, int64_t V, 
   for (int32_t b = 0; b < B; ++b)
     verify_session(T, D, dtype, V, m_offsets, total_drafts, b, draft_tokens, &params[b],
                    session_ids ? session_ids + 16 * (size_t)b : NULL, force_kept,
-                   total_drafts + B, accepted, n_out, out_tokens, status,
+                   total_drafts + B, q_rows, accepted, n_out, out_tokens, status,
                    detail ? &detail[b] : NULL);
   return 0;
 }
@@ -614,8 +637,8 @@ int oracle_verify_batch(const void* T, const void* D, int dtype, int64_t V, int3
                         int32_t* accepted, int32_t* n_out, int32_t* out_tokens,
                         int32_t* status, orc_detail* detail, int nthreads) {
   return oracle_verify_batch_rng(T, D, dtype, V, B, m_offsets, total_drafts, draft_tokens,
-                                 params, NULL, NULL, accepted, n_out, out_tokens, status, detail,
-                                 nthreads);
+                                 params, NULL, NULL, NULL, accepted, n_out, out_tokens, status,
+                                 detail, nthreads);
 }
 
 int oracle_max_threads(void) {

@@ -57,7 +57,7 @@ SessIO make_io(const void* target, const void* draft, int64_t V, int32_t B, cons
   return SessIO{target, draft, V, B, m_offsets, total, tokens, params,
                 reinterpret_cast<const RowStat*>(w + kWsHeader),
                 accepted, n_out, out_tokens, status, reinterpret_cast<const uint32_t*>(w),
-                SDCP_RNG_PHILOX4X32_10, nullptr};
+                SDCP_RNG_PHILOX4X32_10, nullptr, nullptr};
 }
 
 // Clears the header, then launches the row kernel.
@@ -124,6 +124,7 @@ static int verify_sessions(const void* target_logits, const void* draft_logits, 
   if (opts) {
     io.rng = opts->rng_id;
     io.session_ids = opts->session_ids;
+    io.q_rows = opts->q_rows;
   }
   if (launch_sessions(io, dtype, pdl, reinterpret_cast<cudaStream_t>(stream)) != 0) return SDCP_E_LAUNCH;
   return SDCP_OK;
@@ -135,6 +136,7 @@ static int check_options(const sdcp_verify_options* opts) {
   if (opts->struct_size < sizeof(sdcp_verify_options)) return SDCP_E_INVALID;
   if (opts->rng_id != SDCP_RNG_PHILOX4X32_10 && opts->rng_id != SDCP_RNG_HMAC_SHA256) return SDCP_E_INVALID;
   if (opts->rng_id == SDCP_RNG_HMAC_SHA256 && !opts->session_ids) return SDCP_E_INVALID;
+  if (opts->q_rows && ((uintptr_t)opts->q_rows % sizeof(float)) != 0) return SDCP_E_ALIGN;
   return SDCP_OK;
 }
 
@@ -179,9 +181,14 @@ int sdcp_verify_batch_ex(const void* target_logits, const void* draft_logits, in
   rc = check_options(opts);
   if (rc != SDCP_OK) return rc;
   if (B > 0 && (!accepted || !n_out || !out_tokens || !status)) return SDCP_E_INVALID;
-  rc = sdcp_verify_rows(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
-                        draft_tokens, params, workspace, workspace_bytes, stream);
-  if (rc != SDCP_OK || B == 0) return rc;
+  if (B == 0) return SDCP_OK;
+  rc = check_workspace(workspace, workspace_bytes, V, B, total_drafts);
+  if (rc != SDCP_OK) return rc;
+  SessIO io = make_io(target_logits, draft_logits, V, B, m_offsets, total_drafts, draft_tokens, params,
+                      nullptr, nullptr, nullptr, nullptr, workspace);
+  if (opts) io.q_rows = opts->q_rows;
+  rc = launch_rows(io, workspace, nullptr, 0, dtype, reinterpret_cast<cudaStream_t>(stream));
+  if (rc != SDCP_OK) return rc;
   return verify_sessions(target_logits, draft_logits, dtype, V, B, m_offsets, total_drafts,
                          draft_tokens, params, accepted, n_out, out_tokens, status, workspace,
                          workspace_bytes, stream, true, opts);

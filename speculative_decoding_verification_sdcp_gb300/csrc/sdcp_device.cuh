@@ -60,6 +60,7 @@ struct SessIO {
   const uint32_t* error;  // non-zero: a bounded wait of the call gave up
   uint32_t rng;                // SDCP_RNG_*
   const uint8_t* session_ids;  // [B][16] session identifiers (SDCP_RNG_HMAC_SHA256)
+  const float* q_rows;         // [total][V] q as binary32 probabilities, or null (q from logits)
 };
 
 // Arguments of the row kernel.

@@ -345,7 +345,9 @@ __device__ __forceinline__ RowCtx row_ctx(const RowArgs& A, long long row_id, in
   } else {
     const bool rule2 = (P.rule_id == 2u);
     const bool profiled = rule2 || P.rule_id == SDCP_RULE_RELAXED_TOP_K;  // p after the profile
-    skip = !session_ok || (!is_target && !rule2) || (!is_target && A.io.draft == nullptr);
+    // draft rows are read for Rule 2's q from logits only (q given as probability rows, or
+    // no draft logits at all, leaves them unread)
+    skip = !session_ok || (!is_target && (!rule2 || A.io.draft == nullptr || A.io.q_rows != nullptr));
     want_argmax = !profiled || P.temperature_milli == 0u;
     want_profile = profiled && P.temperature_milli != 0u;
   }

@@ -16,6 +16,8 @@
 // (counts per segment, exchange, walk).
 #pragma once
 
+#include <type_traits>
+
 #include "sdcp_device.cuh"
 #include "sdcp_sha256.cuh"
 
@@ -130,7 +132,7 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
   if ((P.rule_id != 1u && P.rule_id != 2u && !relaxed) || P.top_p_milli > 1000u) st = SDCP_S_BAD_PARAMS;
   else if (!offsets_ok) st = SDCP_S_BAD_PARAMS;
   else if (M < 1 || M > SDCP_MAX_M) st = SDCP_S_LIMIT;
-  else if (rule2 && A.draft == nullptr) st = SDCP_S_Q_UNAVAILABLE;
+  else if (rule2 && A.draft == nullptr && A.q_rows == nullptr) st = SDCP_S_Q_UNAVAILABLE;
   if (st == SDCP_S_OK && __ldcg(A.error) != 0u) st = SDCP_S_INTERNAL;
   int a = 0;
   int32_t xr[2] = {-1, -1};
@@ -146,7 +148,24 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
         if (x < 0 || (int64_t)x >= V) range_bad = true;
         const RowStat sp = load_stat(A.stats + off0 + b + i);
         if (sp.flags & (SDCP_ROW_INVALID | SDCP_ROW_SKIPPED)) row_bad = true;
-        if (rule2) {
+        if (rule2 && A.q_rows != nullptr) {
+          // q as given (Section 5.2 q_rows): q(x) must be a probability, and not zero
+          float qx = 0.f;
+          if (x >= 0 && (int64_t)x < V) qx = __ldg(A.q_rows + (size_t)(off0 + i) * (size_t)V + (size_t)x);
+          if (!(qx >= 0.f) || qx == INFINITY) row_bad = true;
+          if (qx == 0.f) q_zero = true;
+          if (tm == 0u) {
+            rej[h] = (x != sp.argmax);
+          } else {
+            // p(x) / q(x) = 2^(dlx_p c) / S_p / q(x)
+            float ratio = 0.f;
+            if ((sp.flags & SDCP_ROW_X_KEPT) && qx > 0.f && qx < INFINITY)
+              ratio = __fdiv_rn(ex2(sp.dlx * c) * __fdiv_rn(1.f, sp.s), qx);
+            ratio = ratio > 1.f ? 1.f : ratio;
+            const double u = session_uniform(A, b, P, (uint32_t)i, 0u);
+            rej[h] = !(u < (double)ratio);
+          }
+        } else if (rule2) {
           const RowStat sq = load_stat(A.stats + R_T + off0 + i);
           if (sq.flags & (SDCP_ROW_INVALID | SDCP_ROW_SKIPPED)) row_bad = true;
           if (!(sq.flags & SDCP_ROW_X_KEPT)) q_zero = true;
@@ -236,18 +255,24 @@ __device__ __forceinline__ float draw_weight(const DrawRow& r, uint32_t bits, in
 
 // Raw words of the 8 ids [j0, j0 + 8) of a row: bf16 one 16-byte vector, fp32 two.  Ids at
 // or past `end` (and every id of a group that is not 16-byte aligned) are read one by one,
-// those past `end` as -inf.
+// those past `end` as `fill`.
 template <typename T> struct Raw8 { static constexpr int W = (sizeof(T) == 2) ? 1 : 2; uint4 v[W]; };
+// q's element type in a draw: the batch's logits type, or binary32 when q is given as rows of
+// probabilities (QR: Section 5.2 q_rows, used as given)
+template <typename T, bool QR> using QElem = typename std::conditional<QR, float, T>::type;
 
+// fill: the bits read for ids at or past `end` (-inf for logits, +0 for q given as
+// probabilities: both are probability 0).
 template <typename T>
-__device__ __forceinline__ void load_raw8(const T* row, bool aligned16, int end, int j0, Raw8<T>& r) {
+__device__ __forceinline__ void load_raw8(const T* row, bool aligned16, int end, int j0, Raw8<T>& r,
+                                          uint32_t fill = 0xFF800000u) {
   if (aligned16 && j0 + kEpt <= end) {
 #pragma unroll
     for (int w = 0; w < Raw8<T>::W; ++w) r.v[w] = __ldg(reinterpret_cast<const uint4*>(row + j0) + w);
   } else {
     uint32_t b[kEpt];
 #pragma unroll
-    for (int e = 0; e < kEpt; ++e) b[e] = (j0 + e < end) ? load_bits(row, j0 + e) : 0xFF800000u;
+    for (int e = 0; e < kEpt; ++e) b[e] = (j0 + e < end) ? load_bits(row, j0 + e) : fill;
     if (sizeof(T) == 2) {
       r.v[0] = make_uint4((b[0] >> 16) | (b[1] & 0xFFFF0000u), (b[2] >> 16) | (b[3] & 0xFFFF0000u),
                           (b[4] >> 16) | (b[5] & 0xFFFF0000u), (b[6] >> 16) | (b[7] & 0xFFFF0000u));
@@ -308,18 +333,18 @@ struct SegSlice {
 };
 
 // Sum of the 8 weights of one lane piece, and the weights themselves.
-template <typename T, bool FILT>
-__device__ __forceinline__ float piece_weights(const Raw8<T>& rp, const Raw8<T>& rq, bool residual,
+template <typename T, bool FILT, bool QR = false>
+__device__ __forceinline__ float piece_weights(const Raw8<T>& rp, const Raw8<QElem<T, QR>>& rq, bool residual,
                                                const DrawRow& pr, const DrawRow& qr, int j0,
                                                float (&w)[kEpt]) {
   uint32_t bp[kEpt], bq[kEpt];
   unpack_raw8<T>(rp, bp);
-  if (residual) unpack_raw8<T>(rq, bq);
+  if (residual) unpack_raw8<QElem<T, QR>>(rq, bq);
   float s = 0.f;
 #pragma unroll
   for (int e = 0; e < kEpt; ++e) {
     float x = draw_weight<FILT>(pr, bp[e], j0 + e);
-    if (residual) x = fmaxf(x - draw_weight<FILT>(qr, bq[e], j0 + e), 0.f);
+    if (residual) x = fmaxf(x - (QR ? __uint_as_float(bq[e]) : draw_weight<FILT>(qr, bq[e], j0 + e)), 0.f);
     w[e] = x;
     s += x;
   }
@@ -327,22 +352,25 @@ __device__ __forceinline__ float piece_weights(const Raw8<T>& rp, const Raw8<T>&
 }
 
 // This CTA's slice: sm.seg[k] = weight of segment group k (ids in order within a group).
-template <typename T, bool FILT>
+template <typename T, bool FILT, bool QR = false>
 __device__ void draw_pass(const SegSlice& sl, SessSmem& sm, const T* prow, const T* qrow, bool residual,
                           bool al_p, bool al_q, int V, const DrawRow& pr, const DrawRow& qr) {
+  using QT = QElem<T, QR>;
+  const QT* qsrc = reinterpret_cast<const QT*>(qrow);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int a, b;
   sl.warp_range(w, kWarps, a, b);
   constexpr int U = (sizeof(T) == 2) ? 4 : 2;  // segments whose loads are in flight together
   float gacc = 0.f;
   for (int k = a; k < b; k += U) {
-    Raw8<T> rp[U], rq[U];
+    Raw8<T> rp[U];
+    Raw8<QT> rq[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int j0 = (k + u) * kSegIds + lane * kEpt;
       if (k + u < b) {
         load_raw8<T>(prow, al_p, V, j0, rp[u]);
-        if (residual) load_raw8<T>(qrow, al_q, V, j0, rq[u]);
+        if (residual) load_raw8<QT>(qsrc, al_q, V, j0, rq[u], QR ? 0u : 0xFF800000u);
       }
     }
 #pragma unroll
@@ -351,11 +379,16 @@ __device__ void draw_pass(const SegSlice& sl, SessSmem& sm, const T* prow, const
       if (kk < b) {
         const int j0 = kk * kSegIds + lane * kEpt;
         float ls = 0.f;
-        for_each8<T>(rp[u], rq[u], [&](uint32_t bp, uint32_t bq, int e) {
-          float x = draw_weight<FILT>(pr, bp, j0 + e);
-          if (residual) x = fmaxf(x - draw_weight<FILT>(qr, bq, j0 + e), 0.f);
-          ls += x;
-        });
+        if constexpr (QR) {
+          float wv[kEpt];
+          ls = piece_weights<T, FILT, true>(rp[u], rq[u], residual, pr, qr, j0, wv);
+        } else {
+          for_each8<T>(rp[u], rq[u], [&](uint32_t bp, uint32_t bq, int e) {
+            float x = draw_weight<FILT>(pr, bp, j0 + e);
+            if (residual) x = fmaxf(x - draw_weight<FILT>(qr, bq, j0 + e), 0.f);
+            ls += x;
+          });
+        }
         gacc += warp_reduce(ls, [](float x, float y) { return x + y; });
         if ((kk - sl.s0 + 1) % sl.G == 0 || kk + 1 == sl.s1) {
           if (lane == 0) sm.seg[(kk - sl.s0) / sl.G] = gacc;
@@ -370,7 +403,7 @@ __device__ void draw_pass(const SegSlice& sl, SessSmem& sm, const T* prow, const
 // cumulative weight exceeds target, else (rounding) the largest id with positive weight seen.
 // Weights and their sums within a segment are fp32; the running total across segments and
 // the comparison with the target are fp64, so long rows keep the position of u * W.
-template <typename T, bool FILT>
+template <typename T, bool FILT, bool QR = false>
 __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p, bool al_q, int V,
                          const DrawRow& pr, const DrawRow& qr, int k0, int k1, double carry,
                          double target) {
@@ -378,11 +411,13 @@ __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p,
   int lastpos = -1;
   for (int k = k0; k < k1; ++k) {
     const int j0 = k * kSegIds + lane * kEpt;
-    Raw8<T> rp, rq;
+    Raw8<T> rp;
+    Raw8<QElem<T, QR>> rq;
     load_raw8<T>(prow, al_p, V, j0, rp);
-    if (residual) load_raw8<T>(qrow, al_q, V, j0, rq);
+    if (residual)
+      load_raw8<QElem<T, QR>>(reinterpret_cast<const QElem<T, QR>*>(qrow), al_q, V, j0, rq, QR ? 0u : 0xFF800000u);
     float wv[kEpt];
-    const float ls = piece_weights<T, FILT>(rp, rq, residual, pr, qr, j0, wv);
+    const float ls = piece_weights<T, FILT, QR>(rp, rq, residual, pr, qr, j0, wv);
     int lp = -1;
 #pragma unroll
     for (int e = 0; e < kEpt; ++e) if (wv[e] > 0.f) lp = j0 + e;
@@ -425,7 +460,7 @@ __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p,
 // as unusable (sm.overflow).  Tie ids come from the CTAs' candidates when `ties`.  Sums
 // within a CTA's slice are fp32 (a scan of at most 2048 segment sums: about 20 roundings);
 // the slices' totals, the target u * W and the owner's base are fp64.
-template <typename T, bool FILT>
+template <typename T, bool FILT, bool QR = false>
 __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                               const SegSlice& sl, const T* prow, const T* qrow, bool residual,
                                               bool al_p, bool al_q, int V, DrawRow pr, DrawRow qr,
@@ -469,8 +504,10 @@ __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, Se
   if (!(W > 0.0)) return W;
   (void)lastr;
   if (owner != (int)rank) return W;
-  pr.tie = pp ? tp_id : INT_MAX;
-  qr.tie = qp ? tq_id : INT_MAX;
+  // tie ids found by this pass (the lists); otherwise the caller's stand (found beforehand
+  // by cut_tie_id, or INT_MAX: every token of the cut value kept)
+  if (pp) pr.tie = tp_id;
+  if (qp) qr.tie = tq_id;
   // the group: the last one with weight whose start is at or below the target (groups tile
   // the slice by construction; a target past the slice's rounded end takes its last group,
   // whose walk then ends on its last token with weight)
@@ -491,7 +528,7 @@ __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, Se
   if (og >= 0 && cand == og) sm.owner_base = obase + (double)cbase;
   g.sync();
   if (w == 0 && og >= 0) {
-    const int tok = draw_walk<T, FILT>(prow, qrow, residual, al_p, al_q, V, pr, qr, sl.grp_lo((int)og),
+    const int tok = draw_walk<T, FILT, QR>(prow, qrow, residual, al_p, al_q, V, pr, qr, sl.grp_lo((int)og),
                                        sl.grp_hi((int)og), sm.owner_base, target);
     if (lane == 0) *out = tok;
   }
@@ -606,7 +643,7 @@ static __device__ bool resolve_ties(cg::cluster_group& cluster, const Group& g, 
 // ---------------------------------------------------------------------------------
 
 // Without cut-value tokens to rank: every token's weight is known during the pass.
-template <typename T, bool FILT>
+template <typename T, bool FILT, bool QR = false>
 __device__ double draw_token(cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                                          const T* prow, const T* qrow, bool residual, bool al_p,
                                          bool al_q, int V, const DrawRow& pr, const DrawRow& qr,
@@ -614,10 +651,10 @@ __device__ double draw_token(cg::cluster_group& cluster, const Group& g, SessSme
   const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
   const SegSlice sl(V, C, rank);
   if (threadIdx.x == 0) { sm.overflow = 0; sm.tie_p_cand = INT_MAX; sm.tie_q_cand = INT_MAX; }
-  draw_pass<T, FILT>(sl, sm, prow, qrow, residual, al_p, al_q, V, pr, qr);
+  draw_pass<T, FILT, QR>(sl, sm, prow, qrow, residual, al_p, al_q, V, pr, qr);
   g.sync();
-  return locate_and_walk<T, FILT>(cluster, g, sm, sl, prow, qrow, residual, al_p, al_q, V, pr, qr,
-                                  false, false, u1, out);
+  return locate_and_walk<T, FILT, QR>(cluster, g, sm, sl, prow, qrow, residual, al_p, al_q, V, pr, qr,
+                                      false, false, u1, out);
 }
 
 // A cut inside a value (p's, q's or both), in one pass; NaN when a list overflowed.
@@ -993,7 +1030,7 @@ __device__ __forceinline__ int kth_qcut(const KeptSmem& K, long long k) {
   return INT_MAX;
 }
 
-template <typename T>
+template <typename T, bool QR = false>
 __device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem& sm, const T* prow,
                            const T* qrow, bool residual, bool al_p, bool al_q, int V, DrawRow pr, DrawRow qr,
                            int np_cut, int nq_cut, double u1, int32_t* out) {
@@ -1085,7 +1122,9 @@ __device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem
   float run = 0.f;
   if (!bad && nc <= kKeptW) {
     if (residual)  // q at the candidates' ids (the loads all in flight at once)
-      for (int i = lane; i < nc; i += 32) K.r[w][i] = __uint_as_float(load_bits(qrow, K.id[w][i]));
+      for (int i = lane; i < nc; i += 32)
+        K.r[w][i] = QR ? __ldg(reinterpret_cast<const float*>(qrow) + K.id[w][i])
+                       : __uint_as_float(load_bits(qrow, K.id[w][i]));
     __syncwarp();
     for (int i0 = 0; i0 < nc; i0 += 32) {
       const int i = i0 + lane;
@@ -1098,8 +1137,12 @@ __device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem
         x = kp ? row_weight(pr, v) : 0.f;
         if (residual && x > 0.f) {
           const float vq = K.r[w][i];
-          const bool kq = vq > qr.thr || (vq == qr.thr && j <= qr.tie);
-          if (kq) x = fmaxf(x - row_weight(qr, vq), 0.f);
+          if (QR) {
+            x = fmaxf(x - vq, 0.f);  // q as given
+          } else {
+            const bool kq = vq > qr.thr || (vq == qr.thr && j <= qr.tie);
+            if (kq) x = fmaxf(x - row_weight(qr, vq), 0.f);
+          }
         }
       }
       float incl = x;
@@ -1166,7 +1209,8 @@ __device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem
 }
 
 // Rule 2's draw for session b whose first rejection is a (a == M: the bonus from p_M).
-template <typename T>
+// QR: q is given as rows of binary32 probabilities (A.q_rows), used as given.
+template <typename T, bool QR = false>
 __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const Group& g, SessSmem& sm,
                              unsigned char* ring, int32_t b, int a) {
   const sdcp_session_params P = A.params[b];
@@ -1178,15 +1222,16 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
   // the residual max(0, p_a - q_a) at Rule 2's first rejection; else a draw from p_a alone
   // (Rule 2's bonus, and every draw of the relaxed rule)
   bool residual = (a < M) && P.rule_id == 2u;
-  const T* drow = residual ? reinterpret_cast<const T*>(A.draft) + (off0 + a) * (int64_t)V
-                           : reinterpret_cast<const T*>(A.target) + (off0 + b + a) * (int64_t)V;
+  const T* drow = !residual ? reinterpret_cast<const T*>(A.target) + (off0 + b + a) * (int64_t)V
+                  : QR ? reinterpret_cast<const T*>(A.q_rows + (off0 + a) * (int64_t)V)
+                       : reinterpret_cast<const T*>(A.draft) + (off0 + a) * (int64_t)V;
   const RowStat sp = load_stat(A.stats + off0 + b + a);
-  const RowStat sq = residual ? load_stat(A.stats + R_T + off0 + a) : sp;
+  const RowStat sq = (residual && !QR) ? load_stat(A.stats + R_T + off0 + a) : sp;
   const float c = profile_c(P.temperature_milli);
   const bool al_p = ((uintptr_t)trow & 15u) == 0, al_q = ((uintptr_t)drow & 15u) == 0;
   const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
   const bool filt_p = sp.thr_key != 0u || sp.thr_n != INT_MAX;
-  const bool filt_q = residual && (sq.thr_key != 0u || sq.thr_n != INT_MAX);
+  const bool filt_q = residual && !QR && (sq.thr_key != 0u || sq.thr_n != INT_MAX);
   DrawRow pr, qr;
   pr.c = qr.c = c;
   pr.lmax = sp.lmax;
@@ -1200,6 +1245,25 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
   const double u1 = session_uniform(A, b, P, (uint32_t)a, 1u);
   int32_t* out = A.out_tokens + off0 + b + a;
   for (int attempt = 0; attempt < 2; ++attempt) {
+    if (QR && residual) {
+      // q as given: p's kept tokens where the slices are short, else a pass from global
+      // memory (p's cut-value tie found first)
+      double W = kNaN64;
+      const int np_cut = sp.thr_n;
+      if (filt_p && (long long)((V + (int)C - 1) / (int)C) * (long long)sizeof(T) <= kKeptSliceBytes)
+        W = draw_kept<T, true>(cluster, g, sm, trow, drow, true, al_p, al_q, V, pr, qr, np_cut, INT_MAX, u1, out);
+      if (W != W) {
+        pr.tie = (np_cut == INT_MAX) ? INT_MAX : cut_tie_id<T>(cluster, g, sm, trow, al_p, V, pr.thr, np_cut);
+        W = filt_p ? draw_token<T, true, true>(cluster, g, sm, trow, drow, true, al_p, al_q, V, pr, qr, u1, out)
+                   : draw_token<T, false, true>(cluster, g, sm, trow, drow, true, al_p, al_q, V, pr, qr, u1, out);
+      }
+      if (!(W > 0.0)) {  // residual mass lost to rounding: use p
+        residual = false;
+        pr.tie = INT_MAX;
+        continue;
+      }
+      break;
+    }
     const bool filt = filt_p || (residual && filt_q);
     const int np_cut = sp.thr_n, nq_cut = residual ? sq.thr_n : INT_MAX;
     const bool ties = np_cut != INT_MAX || nq_cut != INT_MAX;
@@ -1237,7 +1301,7 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
 }
 
 // Verdict in every CTA of the cluster (rank 0 writes it), then the draw if Rule 2 needs one.
-template <typename T>
+template <typename T, bool QR = false>
 __device__ void complete_session(const SessIO& A, cg::cluster_group& cluster, const Group& g,
                                               SessSmem& sm, unsigned char* ring, int32_t b) {
   if ((threadIdx.x >> 5) == 0) {
@@ -1247,7 +1311,7 @@ __device__ void complete_session(const SessIO& A, cg::cluster_group& cluster, co
   g.sync();
   const int a = sm.a, draw = sm.draw;
   g.sync();
-  if (draw) session_draw<T>(A, cluster, g, sm, ring, b, a);  // the same in every CTA of the cluster
+  if (draw) session_draw<T, QR>(A, cluster, g, sm, ring, b, a);  // the same in every CTA of the cluster
 }
 
 }  // namespace sdcp

@@ -12,7 +12,9 @@ namespace sdcp {
 
 constexpr size_t kRingBytes = (size_t)kDrawStages * 2 * kDrawHalf;
 
-template <typename T>
+// QR: q given as rows of binary32 probabilities (a separate instantiation, so that the
+// usual kernel keeps its own register allocation).
+template <typename T, bool QR>
 __global__ void __launch_bounds__(kThreads, 2) session_kernel(SessIO A) {
   extern __shared__ __align__(128) unsigned char ring[];  // the streamed draw's stages
   __shared__ SessSmem sm;
@@ -25,11 +27,13 @@ __global__ void __launch_bounds__(kThreads, 2) session_kernel(SessIO A) {
   }
   __syncthreads();
   pdl_wait_primary();  // the row statistics and the error word are complete from here on
-  complete_session<T>(A, cluster, g, sm, ring, (int32_t)(blockIdx.x / cluster.num_blocks()));
+  complete_session<T, QR>(A, cluster, g, sm, ring, (int32_t)(blockIdx.x / cluster.num_blocks()));
 }
 
-template __global__ void session_kernel<float>(SessIO);
-template __global__ void session_kernel<__nv_bfloat16>(SessIO);
+template __global__ void session_kernel<float, false>(SessIO);
+template __global__ void session_kernel<__nv_bfloat16, false>(SessIO);
+template __global__ void session_kernel<float, true>(SessIO);
+template __global__ void session_kernel<__nv_bfloat16, true>(SessIO);
 
 // CTAs per session: as many as fit two CTAs per SM over the whole batch (a draw is a
 // latency-bound chain, so small batches gain from splitting it), never slices under 16
@@ -53,7 +57,8 @@ cudaError_t session_attributes(int dev) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::call_once(g_once[dev], [&] {
     cudaError_t e = cudaSuccess;
-    const void* fns[2] = {(const void*)session_kernel<__nv_bfloat16>, (const void*)session_kernel<float>};
+    const void* fns[4] = {(const void*)session_kernel<__nv_bfloat16, false>, (const void*)session_kernel<float, false>,
+                          (const void*)session_kernel<__nv_bfloat16, true>, (const void*)session_kernel<float, true>};
     for (const void* fn : fns) {
       if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingBytes);
       if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -86,10 +91,13 @@ int launch_sessions(const SessIO& a, int dtype, bool pdl, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
+  const bool qr = a.q_rows != nullptr;
   if (dtype == SDCP_BF16)
-    e = cudaLaunchKernelEx(&cfg, session_kernel<__nv_bfloat16>, a);
+    e = qr ? cudaLaunchKernelEx(&cfg, session_kernel<__nv_bfloat16, true>, a)
+           : cudaLaunchKernelEx(&cfg, session_kernel<__nv_bfloat16, false>, a);
   else
-    e = cudaLaunchKernelEx(&cfg, session_kernel<float>, a);
+    e = qr ? cudaLaunchKernelEx(&cfg, session_kernel<float, true>, a)
+           : cudaLaunchKernelEx(&cfg, session_kernel<float, false>, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? 0 : (int)e;
 }

@@ -47,7 +47,7 @@ assert COMMIT_PARAMS_DTYPE.itemsize == 48 and STATE_DTYPE.itemsize == 64
 class VerifyOptions(ctypes.Structure):
     """sdcp_verify_options."""
     _fields_ = [("struct_size", ctypes.c_uint32), ("rng_id", ctypes.c_uint32),
-                ("session_ids", ctypes.c_void_p)]
+                ("session_ids", ctypes.c_void_p), ("q_rows", ctypes.c_void_p)]
 
 
 class SdcpError(RuntimeError):
@@ -161,14 +161,19 @@ def sdcp_verify_batch(target_logits, draft_logits, m_offsets, total_drafts, draf
 
 def sdcp_verify_batch_ex(target_logits, draft_logits, m_offsets, total_drafts, draft_tokens,
                          params_dev, accepted, n_out, out_tokens, status, workspace,
-                         rng_id=RNG_PHILOX4X32_10, session_ids=None, stream=None):
+                         rng_id=RNG_PHILOX4X32_10, session_ids=None, q_rows=None, stream=None):
     """sdcp_verify_batch with the random generator chosen by rng_id (session_ids: a device
-    uint8 tensor [B, 16] of session identifiers, for the HMAC-SHA-256 generator)."""
+    uint8 tensor [B, 16] of session identifiers, for the HMAC-SHA-256 generator), and q from
+    the draft logits or from q_rows (a device float32 tensor [total_drafts, V] of the
+    drafter's probabilities)."""
     V = target_logits.shape[1]
     B = accepted.shape[0]
     s = _stream_handle(target_logits.device) if stream is None else ctypes.c_void_p(stream)
+    if q_rows is not None and q_rows.dtype != torch.float32:
+        raise TypeError("q_rows must be torch.float32 probabilities")
     opts = VerifyOptions(ctypes.sizeof(VerifyOptions), int(rng_id),
-                         None if session_ids is None else session_ids.data_ptr())
+                         None if session_ids is None else session_ids.data_ptr(),
+                         None if q_rows is None else q_rows.data_ptr())
     with _on(target_logits):
         rc = lib.sdcp_verify_batch_ex(_ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits),
                                       V, B, _ptr(m_offsets), int(total_drafts), _ptr(draft_tokens),
@@ -272,15 +277,15 @@ class Verifier:
         self.workspace = alloc_workspace(V, B, self.total, self.device)
 
     def __call__(self, target, draft, m_offsets, draft_tokens, params_dev, stream=None,
-                 rng_id=RNG_PHILOX4X32_10, session_ids=None):
-        if rng_id == RNG_PHILOX4X32_10 and session_ids is None:
+                 rng_id=RNG_PHILOX4X32_10, session_ids=None, q_rows=None):
+        if rng_id == RNG_PHILOX4X32_10 and session_ids is None and q_rows is None:
             sdcp_verify_batch(target, draft, m_offsets, self.total, draft_tokens, params_dev,
                               self.accepted, self.n_out, self.out_tokens, self.status,
                               self.workspace, stream)
         else:
             sdcp_verify_batch_ex(target, draft, m_offsets, self.total, draft_tokens, params_dev,
                                  self.accepted, self.n_out, self.out_tokens, self.status,
-                                 self.workspace, rng_id, session_ids, stream)
+                                 self.workspace, rng_id, session_ids, q_rows, stream)
         return self.accepted, self.n_out, self.out_tokens, self.status
 
     def phases(self, target, draft, m_offsets, draft_tokens, params_dev, ev_mid=None):

@@ -185,6 +185,33 @@ def drafter_sample(draft_rows: torch.Tensor, temperature_milli: int, top_k: int,
     return idx.gather(1, pick[:, None]).squeeze(1).to(torch.int32)
 
 
+def drafter_rows(draft_rows: torch.Tensor, temperature_milli: int, top_k: int,
+                 top_p_milli: int) -> torch.Tensor:
+    """The stand-in drafter's distributions over the whole vocabulary, as the binary32 rows it
+    would publish (SDCP Section 5.2 q_rows): the same profile as drafter_sample, in float64,
+    rounded to float32 at the end."""
+    V = draft_rows.shape[1]
+    l = draft_rows.double()
+    out = torch.zeros_like(l)
+    if temperature_milli == 0:
+        out.scatter_(1, torch.argmax(l, dim=1, keepdim=True), 1.0)
+        return out.float()
+    srt, idx = torch.sort(l, dim=1, descending=True, stable=True)
+    k = V if (top_k == 0 or top_k >= V) else top_k
+    srt, idx = srt[:, :k], idx[:, :k]
+    prob = torch.softmax(srt / (temperature_milli / 1000.0), dim=1)
+    if top_p_milli < 1000:
+        cum = torch.cumsum(prob, dim=1)
+        reach = cum >= (top_p_milli / 1000.0)
+        first = torch.where(reach.any(dim=1), reach.int().argmax(dim=1),
+                            torch.full_like(reach[:, 0], k - 1, dtype=torch.long))
+        keep = torch.arange(k, device=l.device)[None, :] <= first[:, None]
+        prob = torch.where(keep, prob, torch.zeros_like(prob))
+        prob = prob / prob.sum(dim=1, keepdim=True)
+    out.scatter_(1, idx, prob)
+    return out.float()
+
+
 def make_batch(w: Workload, device="cpu", max_sessions: int | None = None,
                chunk_rows: int = 256) -> Batch:
     """Build the seeded batch of workload ``w`` on ``device`` (``max_sessions`` trims B)."""

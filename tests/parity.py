@@ -68,15 +68,20 @@ def _sid(session_ids, b):
     return None if session_ids is None else session_ids[b:b + 1]
 
 
+def _qr(q_rows, off, b):
+    return None if q_rows is None else q_rows[int(off[b]):int(off[b + 1])]
+
+
 def session_outputs(got, off, b):
     o0, o1 = int(off[b]), int(off[b + 1])
     return {"status": got["status"][b:b + 1], "accepted": got["accepted"][b:b + 1],
             "n_out": got["n_out"][b:b + 1], "out_tokens": got["out_tokens"][o0 + b:o1 + b + 1]}
 
 
-def _draw_cdf(T, D, off, b, a, prm, mode, force=None):
+def _draw_cdf(T, D, off, b, a, prm, mode, force=None, q_rows=None):
     """Oracle cumulative weights (ids ascending) of the draw of session b at position a
-    (force: top-p crossings per row, in the row order of the C ABI's row statistics)."""
+    (force: top-p crossings per row, in the row order of the C ABI's row statistics; q_rows:
+    q given as probability rows)."""
     s = int(off[b]) + b + a
     d = int(off[b]) + a
     R_T = int(off[-1]) + (off.shape[0] - 1)
@@ -84,7 +89,9 @@ def _draw_cdf(T, D, off, b, a, prm, mode, force=None):
     fp = -1 if force is None else int(force[s])
     fq = -1 if force is None else int(force[R_T + d])
     pa = oracle.row_dist(T[s], tm, k, p, force_kept=fp)[0]
-    qa = oracle.row_dist(D[d], tm, k, p, force_kept=fq)[0] if mode == oracle.EXTRA_RESIDUAL else None
+    qa = None
+    if mode == oracle.EXTRA_RESIDUAL:
+        qa = q_rows[d].astype(np.float64) if q_rows is not None else oracle.row_dist(D[d], tm, k, p, force_kept=fq)[0]
     return oracle.draw_cdf(pa, qa)
 
 
@@ -122,7 +129,7 @@ def _row_margin(info):
                abs(info.topp_cum_before - info.topp_target)) / info.topp_target
 
 
-def _forced_session(T, D, off, x, params, b, gs, session_ids=None):
+def _forced_session(T, D, off, x, params, b, gs, session_ids=None, q_rows=None):
     """The oracle on session b alone with the GPU's top-p crossings at the session's
     boundary rows (each checked to lie in its band)."""
     B = params.shape[0]
@@ -144,7 +151,8 @@ def _forced_session(T, D, off, x, params, b, gs, session_ids=None):
         lo, hi = topp_band(logits, tm, k, p)
         assert lo <= n <= hi, ("session %d row %d: GPU crossing %d outside the band [%d, %d]" % (b, r, n, lo, hi))
         force[j] = n
-    return args, force, oracle.verify_batch(*args, force_kept=force, session_ids=_sid(session_ids, b))
+    return args, force, oracle.verify_batch(*args, force_kept=force, session_ids=_sid(session_ids, b),
+                                            q_rows=_qr(q_rows, off, b))
 
 
 def _draw_diagnostics(T, D, off, params, b, a, mode, gs, det, force):
@@ -189,7 +197,7 @@ def _draw_diagnostics(T, D, off, params, b, a, mode, gs, det, force):
 
 
 def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None, force=None,
-                     session_ids=None):
+                     session_ids=None, q_rows=None):
     """One session; adds to counts; raises AssertionError on a real disagreement.  force:
     the top-p crossings ref was computed with (None: as defined)."""
     det = ref["detail"]
@@ -210,11 +218,11 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
         # the oracle under one of the band's two ends
         mine = session_outputs(got, off, b)
         if gs is not None:
-            args, force2, r2 = _forced_session(T, D, off, x, params, b, gs, session_ids)
+            args, force2, r2 = _forced_session(T, D, off, x, params, b, gs, session_ids, q_rows)
             c2 = {"exact": 0, "accept_boundary": 0, "draw_boundary": 0, "topp_boundary": 0}
             try:
                 _compare_session(mine, r2, *args, 0, c2, topp_ok=False, force=force2,
-                                 session_ids=_sid(session_ids, b))
+                                 session_ids=_sid(session_ids, b), q_rows=_qr(q_rows, off, b))
             except AssertionError as e:
                 a = int(got["accepted"][b])
                 mode = int(r2["detail"]["extra_mode"][0])
@@ -227,10 +235,10 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
         for shift in (-BOUNDARY, BOUNDARY):
             c2 = {"exact": 0, "accept_boundary": 0, "draw_boundary": 0, "topp_boundary": 0}
             with oracle.topp_shift(shift):
-                r2 = oracle.verify_batch(*args, session_ids=_sid(session_ids, b))
+                r2 = oracle.verify_batch(*args, session_ids=_sid(session_ids, b), q_rows=_qr(q_rows, off, b))
                 try:
                     _compare_session(mine, r2, *args, 0, c2, topp_ok=False,
-                                     session_ids=_sid(session_ids, b))
+                                     session_ids=_sid(session_ids, b), q_rows=_qr(q_rows, off, b))
                 except AssertionError as e:
                     errs.append(str(e))
                     continue
@@ -255,7 +263,7 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
     assert mode in (oracle.EXTRA_RESIDUAL, oracle.EXTRA_BONUS, oracle.EXTRA_RESIDUAL_AS_P,
                     oracle.EXTRA_FROM_P), mode
     m2 = oracle.EXTRA_RESIDUAL if mode == oracle.EXTRA_RESIDUAL else oracle.EXTRA_BONUS
-    C, W = _draw_cdf(T, D, off, b, a, params[b], m2, force)
+    C, W = _draw_cdf(T, D, off, b, a, params[b], m2, force, q_rows)
     try:
         _check_draw_boundary(C, W, float(det["u1"][b]), int(gt[a]), int(rt[a]), b)
     except AssertionError as e:
@@ -266,7 +274,7 @@ def _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok, gs=None
                           ref["out_tokens"][o0 + b + a + 1:o1 + b + 1])
 
 
-def compare_verdicts(got, ref, T, D, off, x, params, gs=None, session_ids=None):
+def compare_verdicts(got, ref, T, D, off, x, params, gs=None, session_ids=None, q_rows=None):
     """Returns a dict of counts; raises AssertionError on a real disagreement.  gs: the
     GPU's row statistics of the same batch (sdcp_row_stats), used where a top-p crossing
     lies within rounding of P."""
@@ -276,7 +284,7 @@ def compare_verdicts(got, ref, T, D, off, x, params, gs=None, session_ids=None):
     assert np.array_equal(got["status"], ref["status"]), (got["status"], ref["status"])
     for b in range(B):
         _compare_session(got, ref, T, D, off, x, params, b, counts, topp_ok=True, gs=gs,
-                         session_ids=session_ids)
+                         session_ids=session_ids, q_rows=q_rows)
     return counts
 
 

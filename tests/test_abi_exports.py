@@ -42,7 +42,7 @@ def test_host_only_calls(libsdcp):
     libsdcp.sdcp_strerror.restype = ctypes.c_char_p
     libsdcp.sdcp_workspace_bytes.restype = ctypes.c_size_t
     libsdcp.sdcp_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int64]
-    assert libsdcp.sdcp_abi_version() == 1
+    assert libsdcp.sdcp_abi_version() == 2
     assert b"success" in libsdcp.sdcp_strerror(0)
     assert libsdcp.sdcp_workspace_bytes(32000, 64, 512) >= (2 * 512 + 64) * 32
     assert libsdcp.sdcp_workspace_bytes(0, 64, 512) == 0

@@ -626,3 +626,75 @@ def test_relaxed_rule_accepts_by_rank(oracle_mod, k):
         row = T[o0 + b + a]
         rank = int((row > row[extra]).sum() + ((row == row[extra]) & (np.arange(row.shape[0]) < extra)).sum())
         assert rank < k
+
+
+# ---------------------------------------------------------------------------------------
+# q given as rows of probabilities (SDCP Section 5.2 q_rows)
+# ---------------------------------------------------------------------------------------
+@pytest.mark.parametrize("M", [1, 2])
+def test_q_rows_output_distribution_is_p(oracle_mod, M):
+    """With q given as probability rows (any distribution the tokens are drawn from), the
+    first emitted token ~ p[0] and, after an accepted first token, the next ~ p[1]."""
+    rng = np.random.default_rng(40 + M)
+    V = 5
+    tl = [np.array([1.0, 0.2, -0.5, 0.7, -1.0], np.float32),
+          np.array([-0.3, 1.1, 0.4, -0.8, 0.0], np.float32),
+          np.array([0.5, -0.5, 1.5, 0.1, -2.0], np.float32)]
+    qr = np.array([[0.125, 0.5, 0.0625, 0.25, 0.0625],
+                   [0.25, 0.125, 0.5, 0.0625, 0.0625]], np.float32)  # exact in binary32
+    Bn = 60000
+    prm = _params(oracle_mod, Bn, rule=2, T=1000)
+    prm["seed"] = np.arange(Bn, dtype=np.uint64) * 7919 + 13
+    target = np.concatenate([np.stack(tl[:M + 1])] * Bn)
+    q_rows = np.concatenate([qr[:M]] * Bn)
+    off = _offsets([M] * Bn)
+    p = [oracle_mod.row_dist(t)[0] for t in tl[:M + 1]]
+    toks = np.stack([rng.choice(V, size=Bn, p=qr[i].astype(np.float64)) for i in range(M)], axis=1)
+    toks = toks.reshape(-1).astype(np.int32)
+    res = oracle_mod.verify_batch(target, None, off, toks, prm, nthreads=8, want_detail=False, q_rows=q_rows)
+    assert (res["status"] == 0).all()
+    out = res["out_tokens"].reshape(Bn, M + 1)
+    c2, dof = _chi2(np.bincount(out[:, 0], minlength=V), p[0])
+    assert c2 < 30, c2
+    sel = res["n_out"] >= 2
+    c2b, _ = _chi2(np.bincount(out[sel, 1], minlength=V), p[1])
+    assert c2b < 30, c2b
+
+
+def test_q_rows_equal_to_p_accept_everything(oracle_mod):
+    """q_rows holding p itself (fp64 -> binary32): the ratio is 1 up to rounding, so every
+    proposal of a token with p(x) > 0 is accepted unless u lies within rounding of 1."""
+    rng = np.random.default_rng(5)
+    B, V, M = 40, 30, 3
+    off = _offsets([M] * B)
+    T = rng.normal(0, 2, size=(B * M + B, V)).astype(np.float32)
+    rows = np.arange(B * M) + np.repeat(np.arange(B), M)
+    q_rows = np.stack([oracle_mod.row_dist(T[r], 800)[0] for r in rows]).astype(np.float32)
+    x = np.array([rng.choice(V, p=q / q.sum()) for q in q_rows.astype(np.float64)], np.int32)
+    res = oracle_mod.verify_batch(T, None, off, x, _params(oracle_mod, B, rule=2, T=800), q_rows=q_rows)
+    det = res["detail"]
+    for b in range(B):
+        a = int(res["accepted"][b])
+        if a < M:  # a rejection can only come from a uniform within rounding of the ratio
+            assert abs(det["u0"][b][a] - det["ratio"][b][a]) < 1e-6, (b, a)
+
+
+def test_q_rows_statuses(oracle_mod):
+    """q(x) = 0 is a bad proposal; a q(x) that is not a probability (NaN, infinite or
+    negative) gives no distribution; Rule 2 needs neither draft logits nor a profile on q."""
+    rng = np.random.default_rng(6)
+    B, V, M = 5, 8, 2
+    off = _offsets([M] * B)
+    T = rng.normal(0, 1, size=(B * M + B, V)).astype(np.float32)
+    q_rows = np.full((B * M, V), 1.0 / V, np.float32)
+    x = np.zeros(B * M, np.int32)
+    q_rows[2, 0] = 0.0            # session 1, position 0
+    q_rows[5, 0] = np.nan         # session 2, position 1
+    q_rows[6, 0] = -0.25          # session 3, position 0
+    q_rows[9, 0] = np.inf         # session 4, position 1
+    res = oracle_mod.verify_batch(T, None, off, x, _params(oracle_mod, B, rule=2), q_rows=q_rows)
+    S = oracle_mod
+    assert list(res["status"]) == [S.S_OK, S.S_BAD_PROPOSAL, S.S_BAD_PARAMS, S.S_BAD_PARAMS, S.S_BAD_PARAMS]
+    # without q_rows and without draft logits the same sessions have no q at all
+    res2 = oracle_mod.verify_batch(T, None, off, x, _params(oracle_mod, B, rule=2))
+    assert (res2["status"] == S.S_Q_UNAVAILABLE).all()
