@@ -54,6 +54,8 @@ struct RowPlan {
   long long row_id;  // < 0: no more work for the CTA
   int nchunks;
   int32_t xt;        // the row's draft token as the token array holds it (-1: none)
+  bool skip;         // the row needs no statistics (its first stage was copied before that was
+                     // known): the consumers hand the stage back and record it as skipped
   RowCtx x;
 };
 
@@ -973,56 +975,68 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
     uint32_t phase = 0;
     bool ok = true;
     uint32_t issued = 0u, issued_par = 0u;  // lane 0: stages with a copy issued, and its parity
+    // rows 0 .. gridDim.x - 1 go to the CTAs of the same index; later ones are claimed
     auto fetch = [&]() -> long long {
       unsigned long long r = 0;
       if (l == 0) r = atomicAdd(&A.hdr->next_slot, 1ull);
-      return (long long)__shfl_sync(0xFFFFFFFFu, r, 0);
+      return (long long)gridDim.x + (long long)__shfl_sync(0xFFFFFFFFu, r, 0);
     };
-    long long rcur = fetch();
-    SlotInfo cur = resolve_row<T>(A, rcur);
+    const long long R_T = A.io.total + A.io.B;
+    long long rcur = blockIdx.x;
     while (ok && rcur < nrows) {
-      if (cur.skip) {
-        if (l == 0) write_skipped(A, cur.row_id);
-        rcur = fetch();
+      // A target row is copied before its session is looked up: its address needs no
+      // context, the lookup then runs while the copy is in flight, and the row's plan is
+      // published by the producer's arrival, which the stage's phase needs besides the copy's
+      // bytes (an mbarrier's transaction count may go below zero until that arrival).  A
+      // draft row is looked up first: a draft row that needs no statistics is not read.
+      const bool early = rcur < R_T;
+      SlotInfo cur;
+      cur.row_id = rcur;
+      cur.skip = false;
+      cur.xt = -1;
+      if (!early) {
         cur = resolve_row<T>(A, rcur);
-        continue;
+        if (cur.skip) {
+          if (l == 0) write_skipped(A, cur.row_id);
+          rcur = fetch();
+          continue;
+        }
       }
-      const T* row = row_ptr<T>(A, cur.row_id);
+      const T* row = row_ptr<T>(A, rcur);
       const RowLayout L = row_layout(row, A.io.V);
       const long long vbytes = L.nvec * 16;
       const int nch = (int)max(1ll, (vbytes + kChunk - 1) / kChunk);
       const char* src = reinterpret_cast<const char*>(row + L.head);
       long long rnext = nrows;
-      SlotInfo nxt;
-      nxt.row_id = -1;
-      nxt.skip = true;
-      nxt.xt = -1;
       for (int c = 0; c < nch && ok; ++c) {
-        if (l == 0) {
-          if (!mbar_wait_spin(&sh.empty[stage], phase ^ 1u, &sh.abort) || sh.abort) {
-            ok = false;
-          } else {
-            const long long off = (long long)c * kChunk;
-            const uint32_t bytes = (uint32_t)max(0ll, min((long long)kChunk, vbytes - off));
-            if (c == 0) sh.plan[stage] = RowPlan{cur.row_id, nch, cur.xt, cur.x};
-            mbar_arrive_expect_tx(&sh.full[stage], bytes);
-            if (bytes > 0) bulk_copy_g2s(ring + (size_t)stage * kChunk, src + off, bytes, &sh.full[stage]);
-            issued |= 1u << stage;
-            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-          }
-        }
+        const long long off = (long long)c * kChunk;
+        const uint32_t bytes = (uint32_t)max(0ll, min((long long)kChunk, vbytes - off));
+        if (l == 0 && (!mbar_wait_spin(&sh.empty[stage], phase ^ 1u, &sh.abort) || sh.abort)) ok = false;
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+        if (!ok) break;
+        const bool first_early = (c == 0) && early;
+        if (l == 0) {
+          if (first_early && bytes > 0) bulk_copy_g2s(ring + (size_t)stage * kChunk, src, bytes, &sh.full[stage]);
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        }
+        if (first_early) cur = resolve_row<T>(A, rcur);  // whole warp, the copy in flight
+        const bool stop = first_early && cur.skip;       // only this stage was copied
+        if (l == 0) {
+          if (c == 0) sh.plan[stage] = RowPlan{cur.row_id, stop ? 1 : nch, cur.xt, stop, cur.x};
+          mbar_arrive_expect_tx(&sh.full[stage], bytes);
+          if (!first_early && bytes > 0)
+            bulk_copy_g2s(ring + (size_t)stage * kChunk, src + off, bytes, &sh.full[stage]);
+        }
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
-        // the next row once this row's last stage is issued (its copies and the stages
-        // queued before it cover the lookup); claiming earlier would let a busy CTA hold a
-        // row that an idle one could take, which lengthens the tail
-        if (c == nch - 1 && ok) {
+        // the next row once this row's last stage is issued; claiming earlier would let a
+        // busy CTA hold a row that an idle one could take, which lengthens the tail
+        if (c == nch - 1 || stop) {
           rnext = fetch();
-          nxt = resolve_row<T>(A, rnext);
+          break;
         }
       }
       rcur = rnext;
-      cur = nxt;
     }
     if (l == 0) {
       if (ok && mbar_wait_for(&sh.empty[stage], phase ^ 1u, &sh.abort) && !sh.abort) {
@@ -1052,6 +1066,13 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
       if (sh.abort) break;
       const RowPlan plan = sh.plan[stage];
       if (plan.row_id < 0) break;
+      if (plan.skip) {  // copied before it was known to need nothing
+        __syncwarp();
+        if (l == 0) mbar_arrive(&sh.empty[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (t == 0) write_skipped(A, plan.row_id);
+        continue;
+      }
       const RowCtx& x = plan.x;
       const T* row = row_ptr<T>(A, plan.row_id);
       const RowLayout L = row_layout(row, A.io.V);

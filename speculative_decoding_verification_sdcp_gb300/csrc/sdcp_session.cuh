@@ -31,6 +31,7 @@ constexpr int kDrawHalf = 16384;    // bytes of p (and of q) per stage of the st
 constexpr int kDrawStages = 2;      // stages of the streamed draw's ring
 constexpr int kKeptW = 128;         // candidates (p's kept tokens) per warp: kept-set draw
 constexpr int kQCutW = 32;          // q's cut-value ids per warp: kept-set draw
+constexpr int kMaxCluster = 8;     // CTAs per session cluster at most
 constexpr int kKeptSliceBytes = 65536;  // largest slice of p a CTA scans with plain loads
 #define kNaN64 __longlong_as_double(0x7FF8000000000000ll)  // "the draw could not decide"
 
@@ -63,6 +64,7 @@ struct SessSmem {
     KeptSmem kept;                   // the kept-set draw
   };
   int tie_n[kWarps];
+  uint8_t plist[kWarps][kDrawHalf / kEpt / kWarps / 2];  // per warp: the stage's pieces to weigh
   int tsc_p[kTieStages][kWarps], tsc_q[kTieStages][kWarps];  // cut-value tokens per stage, warp
   int overflow;
   long long cta_np, cta_nq;  // cut-value tokens of the slice (read by the cluster)
@@ -77,7 +79,21 @@ struct SessSmem {
   long long result;    // a tie id found by this CTA (read by the cluster)
   int st, a, draw;
   uint32_t ring_uses;  // stages of the draw ring used so far (slot and barrier parity)
+  // local copies of the cluster's per-CTA values (lane r of warp 0 reads rank r, so each
+  // value crosses the cluster once per CTA, not once per thread)
+  double cv_sum[kMaxCluster];
+  long long cv_n0[kMaxCluster], cv_n1[kMaxCluster];
+  int cv_ovf[kMaxCluster], cv_i0[kMaxCluster], cv_i1[kMaxCluster];
+  long long cv_res;
 };
+
+// Lanes r < C of warp 0: dst[r] = the value at src in the shared memory of cluster rank r.
+// Between two cluster barriers: the first publishes src, the second orders dst before its
+// readers (and keeps every CTA's src alive until the cluster has read it).
+template <typename V>
+__device__ __forceinline__ void cluster_copy(cg::cluster_group& cluster, V* src, V* dst) {
+  if (threadIdx.x < cluster.num_blocks()) dst[threadIdx.x] = *cluster.map_shared_rank(src, threadIdx.x);
+}
 
 // Verdict of a session: status, accepted count, and whether Rule 2 still draws a token.
 struct Verdict {
@@ -295,6 +311,37 @@ __device__ __forceinline__ void unpack_raw8(const Raw8<T>& r, uint32_t (&b)[kEpt
   }
 }
 
+// Whether some value of a piece is >= thr (bf16: packed maxima; -inf pads count as below).
+template <typename T>
+__device__ __forceinline__ bool piece_reaches(const Raw8<T>& r, float thr) {
+  if constexpr (sizeof(T) == 2) {
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&r.v[0].x),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&r.v[0].y));
+    const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&r.v[0].z),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&r.v[0].w));
+    const __nv_bfloat162 ab = __hmax2(a, b);
+    const uint32_t m = *reinterpret_cast<const uint32_t*>(&ab);
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u)) >= thr;
+  } else {
+    float m = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < Raw8<T>::W; ++w)
+      m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(r.v[w].x), __uint_as_float(r.v[w].y)),
+                         fmaxf(__uint_as_float(r.v[w].z), __uint_as_float(r.v[w].w))));
+    return m >= thr;
+  }
+}
+// Whether some value of a piece equals v.
+template <typename T>
+__device__ __forceinline__ bool piece_holds(const Raw8<T>& r, float v) {
+  uint32_t b[kEpt];
+  unpack_raw8<T>(r, b);
+  bool h = false;
+#pragma unroll
+  for (int e = 0; e < kEpt; ++e) h |= (__uint_as_float(b[e]) == v);
+  return h;
+}
+
 // f(bits of p, bits of q, e) for the 8 elements of one lane piece, in id order, straight from
 // the loaded words (no per-element arrays: they would not fit the register budget).
 template <typename T, typename F>
@@ -477,16 +524,19 @@ __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, Se
   const float pre = group_excl_scan(g, loc, sm.fscr, &Wc);
   if (t == 0) { sm.cta_sum = (double)Wc; sm.cta_ovf = sm.overflow; }
   cluster.sync();
+  cluster_copy(cluster, &sm.cta_sum, sm.cv_sum);
+  cluster_copy(cluster, &sm.tie_p_cand, sm.cv_i0);
+  cluster_copy(cluster, &sm.tie_q_cand, sm.cv_i1);
+  cluster_copy(cluster, &sm.cta_ovf, sm.cv_ovf);
+  cluster.sync();  // every CTA has read the slice totals
   double W = 0.0;
-  int owner = -1, lastr = -1, tp_id = INT_MAX, tq_id = INT_MAX, bad = 0;
+  int owner = -1, tp_id = INT_MAX, tq_id = INT_MAX, bad = 0;
   double obase = 0.0;
   for (unsigned r = 0; r < C; ++r) {
-    const double sr = *cluster.map_shared_rank(&sm.cta_sum, r);
-    if (sr > 0.0) lastr = (int)r;
-    W += sr;
-    tp_id = min(tp_id, *cluster.map_shared_rank(&sm.tie_p_cand, r));
-    tq_id = min(tq_id, *cluster.map_shared_rank(&sm.tie_q_cand, r));
-    bad |= *cluster.map_shared_rank(&sm.cta_ovf, r);
+    W += sm.cv_sum[r];
+    tp_id = min(tp_id, sm.cv_i0[r]);
+    tq_id = min(tq_id, sm.cv_i1[r]);
+    bad |= sm.cv_ovf[r];
   }
   const double target = u1 * W;
   {
@@ -494,15 +544,13 @@ __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, Se
     // slices tile [0, W) by construction, whatever the rounding of their sums)
     double acc = 0.0;
     for (unsigned r = 0; r < C; ++r) {
-      const double sr = *cluster.map_shared_rank(&sm.cta_sum, r);
+      const double sr = sm.cv_sum[r];
       if (sr > 0.0 && acc <= target) { owner = (int)r; obase = acc; }
       acc += sr;
     }
   }
-  cluster.sync();  // every CTA has read the slice totals
   if (bad) return kNaN64;
   if (!(W > 0.0)) return W;
-  (void)lastr;
   if (owner != (int)rank) return W;
   // tie ids found by this pass (the lists); otherwise the caller's stand (found beforehand
   // by cut_tie_id, or INT_MAX: every token of the cut value kept)
@@ -611,13 +659,16 @@ static __device__ bool resolve_ties(cg::cluster_group& cluster, const Group& g, 
     sm.cta_np = ap; sm.cta_nq = aq; sm.cta_ovf = sm.overflow;
   }
   cluster.sync();
+  cluster_copy(cluster, &sm.cta_np, sm.cv_n0);
+  cluster_copy(cluster, &sm.cta_nq, sm.cv_n1);
+  cluster_copy(cluster, &sm.cta_ovf, sm.cv_ovf);
+  cluster.sync();  // every CTA has read the counts
   long long P0 = 0, Q0 = 0;
   int ovf_any = 0;
   for (unsigned r = 0; r < C; ++r) {
-    if (r < rank) { P0 += *cluster.map_shared_rank(&sm.cta_np, r); Q0 += *cluster.map_shared_rank(&sm.cta_nq, r); }
-    ovf_any |= *cluster.map_shared_rank(&sm.cta_ovf, r);
+    if (r < rank) { P0 += sm.cv_n0[r]; Q0 += sm.cv_n1[r]; }
+    ovf_any |= sm.cv_ovf[r];
   }
-  cluster.sync();  // every CTA has read the counts
   if (ovf_any) return false;
   TieEntry* L = sm.ties[w];
   const int nt = sm.tie_n[w];
@@ -752,6 +803,7 @@ __device__ double draw_stream(cg::cluster_group& cluster, const Group& g, SessSm
   constexpr int S = kDrawHalf / (int)sizeof(T);  // ids per stage
   constexpr int SPW = S / kSegIds / kWarps;       // segments of a warp per stage
   static_assert(SPW >= 1 && SPW * kWarps * kSegIds == S, "stage layout");
+  static_assert(SPW * 32 <= (int)sizeof(sm.plist[0]), "piece list");
   const int lo = sl.s0 * kSegIds, hi = min(sl.s1 * kSegIds, V);
   const int nst = (hi > lo) ? (hi - lo + S - 1) / S : 0;
   const bool pp = TIES && np_cut != INT_MAX, qp = TIES && residual && nq_cut != INT_MAX;
@@ -788,22 +840,18 @@ __device__ double draw_stream(cg::cluster_group& cluster, const Group& g, SessSm
     if (!mbar_wait_for(&sm.full[slot], (u / kDrawStages) & 1u, nullptr)) fail = true;
     const unsigned char* src = ring + (size_t)slot * 2 * kDrawHalf;
     const int stage_lo = lo + s * S;
-#pragma unroll 1
-    for (int i = 0; i < SPW; ++i) {
-      const int sis = w * SPW + i;  // segment in the stage
-      const int seg_lo = stage_lo + sis * kSegIds;
-      if (seg_lo >= hi) continue;  // past the slice (warp-uniform)
-      const int j0 = seg_lo + lane * kEpt;
-      Raw8<T> rp, rq;
-      const uint4* pv = reinterpret_cast<const uint4*>(src + (size_t)(sis * kSegIds + lane * kEpt) * sizeof(T));
+    // the lane's piece (8 ids) of segment sis of the stage; ids past the slice read as -inf
+    auto load_piece = [&](int sis, int pl, Raw8<T>& rp, Raw8<T>& rq) {
+      const int j0 = stage_lo + sis * kSegIds + pl * kEpt;
+      const uint4* pv = reinterpret_cast<const uint4*>(src + (size_t)(sis * kSegIds + pl * kEpt) * sizeof(T));
 #pragma unroll
       for (int q = 0; q < Raw8<T>::W; ++q) rp.v[q] = pv[q];
       if (residual) {
-        const uint4* qv = reinterpret_cast<const uint4*>(src + kDrawHalf + (size_t)(sis * kSegIds + lane * kEpt) * sizeof(T));
+        const uint4* qv = reinterpret_cast<const uint4*>(src + kDrawHalf + (size_t)(sis * kSegIds + pl * kEpt) * sizeof(T));
 #pragma unroll
         for (int q = 0; q < Raw8<T>::W; ++q) rq.v[q] = qv[q];
       }
-      if (j0 + kEpt > hi) {  // the row's last segment: ids past V read as -inf
+      if (j0 + kEpt > hi) {  // the row's last segment
         uint32_t* a = reinterpret_cast<uint32_t*>(rp.v);
         uint32_t* bq = reinterpret_cast<uint32_t*>(rq.v);
 #pragma unroll
@@ -819,8 +867,11 @@ __device__ double draw_stream(cg::cluster_group& cluster, const Group& g, SessSm
           }
         }
       }
-      uint32_t amb = 0u, cp = 0u, cq = 0u;
-      float ls = 0.f;
+      return j0;
+    };
+    // the weights of one piece: ls (tokens off the cut values), amb / cp / cq (on them)
+    auto weigh = [&](const Raw8<T>& rp, const Raw8<T>& rq, int j0, float& ls, uint32_t& amb, uint32_t& cp,
+                     uint32_t& cq) {
       for_each8<T>(rp, rq, [&](uint32_t bp, uint32_t bqq, int e) {
         if (!TIES) {
           float x = draw_weight<FILT>(pr, bp, j0 + e);
@@ -838,10 +889,72 @@ __device__ double draw_stream(cg::cluster_group& cluster, const Group& g, SessSm
           ls += am ? 0.f : x;
         }
       });
-      const float ssum = warp_reduce(ls, [](float x, float y) { return x + y; });
-      if (lane == 0) sm.seg[(seg_lo - lo) / kSegIds] = ssum;
-      if (TIES && __any_sync(0xFFFFFFFFu, amb != 0u))
-        tie_append<T>(sm, rp, rq, residual, pr, qr, j0, amb, cp, cq, s, nt, ovf);
+    };
+    if constexpr (!FILT) {
+#pragma unroll 1
+      for (int i = 0; i < SPW; ++i) {
+        const int sis = w * SPW + i;  // segment in the stage
+        const int seg_lo = stage_lo + sis * kSegIds;
+        if (seg_lo >= hi) continue;  // past the slice (warp-uniform)
+        Raw8<T> rp, rq;
+        const int j0 = load_piece(sis, lane, rp, rq);
+        uint32_t amb = 0u, cp = 0u, cq = 0u;
+        float ls = 0.f;
+        weigh(rp, rq, j0, ls, amb, cp, cq);
+        const float ssum = warp_reduce(ls, [](float x, float y) { return x + y; });
+        if (lane == 0) sm.seg[(seg_lo - lo) / kSegIds] = ssum;
+      }
+    } else {
+      // p has a cut: a piece whose p values all lie below p's cut value weighs nothing (p is
+      // 0 there, so is the residual), and holds no cut-value token of p.  Only the pieces
+      // that reach p's cut value, or hold a token on q's cut value (whose ranks the ties
+      // need), are weighed: listed per warp in id order, then taken one per lane.
+      uint32_t mk = 0u;
+#pragma unroll
+      for (int i = 0; i < SPW; ++i) {
+        const int sis = w * SPW + i;
+        if (stage_lo + sis * kSegIds >= hi) continue;  // warp-uniform
+        Raw8<T> rp, rq;
+        (void)load_piece(sis, lane, rp, rq);
+        bool m = piece_reaches<T>(rp, pr.thr);
+        if (TIES && qp) m = m || piece_holds<T>(rq, qr.thr);
+        mk |= (m ? 1u : 0u) << i;
+      }
+      uint8_t* list = sm.plist[w];
+      int H = 0;
+#pragma unroll
+      for (int i = 0; i < SPW; ++i) {
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, (mk >> i) & 1u);
+        if ((mk >> i) & 1u) list[H + __popc(bal & ((1u << lane) - 1u))] = (uint8_t)(i * 32 + lane);
+        H += __popc(bal);
+      }
+      __syncwarp();
+      float segsum[SPW];
+#pragma unroll
+      for (int i = 0; i < SPW; ++i) segsum[i] = 0.f;
+      for (int e0 = 0; e0 < H; e0 += 32) {
+        const int e = e0 + lane;
+        Raw8<T> rp, rq;
+        uint32_t amb = 0u, cp = 0u, cq = 0u;
+        float ls = 0.f;
+        int pi = -1, j0 = 0;
+        if (e < H) {
+          pi = list[e];
+          j0 = load_piece(w * SPW + (pi >> 5), pi & 31, rp, rq);
+          weigh(rp, rq, j0, ls, amb, cp, cq);
+        }
+#pragma unroll
+        for (int i = 0; i < SPW; ++i) segsum[i] += (pi >= 0 && (pi >> 5) == i) ? ls : 0.f;
+        if (TIES && __any_sync(0xFFFFFFFFu, amb != 0u))
+          tie_append<T>(sm, rp, rq, residual, pr, qr, j0, amb, cp, cq, s, nt, ovf);
+      }
+      __syncwarp();  // the list is free for the next stage
+#pragma unroll
+      for (int i = 0; i < SPW; ++i) {
+        const int seg_lo = stage_lo + (w * SPW + i) * kSegIds;
+        const float ssum = warp_reduce(segsum[i], [](float x, float y) { return x + y; });
+        if (lane == 0 && seg_lo < hi) sm.seg[(seg_lo - lo) / kSegIds] = ssum;
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[slot]);
@@ -909,10 +1022,12 @@ __device__ int cut_tie_id(cg::cluster_group& cluster, const Group& g, SessSmem& 
   const long long pre = group_excl_scan_ll(g, loc, sm.lscr, &tot);
   if (t == 0) sm.cta_cnt = tot;
   cluster.sync();
+  cluster_copy(cluster, &sm.cta_cnt, sm.cv_n0);
+  g.sync();  // the copies, before their readers (sm.cta_cnt is not written again in this call)
   long long base = 0, acc = 0;
   int owner = -1;
   for (unsigned r = 0; r < C; ++r) {
-    const long long cr = *cluster.map_shared_rank(&sm.cta_cnt, r);
+    const long long cr = sm.cv_n0[r];
     if (r == rank) base = acc;
     if (owner < 0 && acc < n && n <= acc + cr) owner = (int)r;
     acc += cr;
@@ -962,8 +1077,9 @@ __device__ int cut_tie_id(cg::cluster_group& cluster, const Group& g, SessSmem& 
     }
   }
   cluster.sync();
-  const long long id = (owner >= 0) ? *cluster.map_shared_rank(&sm.result, (unsigned)owner) : LLONG_MAX;
+  if (t == 0) sm.cv_res = (owner >= 0) ? *cluster.map_shared_rank(&sm.result, (unsigned)owner) : LLONG_MAX;
   cluster.sync();  // the owner's shared memory is read before anyone moves on
+  const long long id = sm.cv_res;
   return (id == LLONG_MAX || id == INT_MAX) ? INT_MAX : (int)id;
 }
 
@@ -1094,11 +1210,15 @@ __device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem
   bool bad = false;
   if (pp || qp) {  // the ids of the np_cut-th / nq_cut-th cut-value tokens over the cluster
     cluster.sync();
+    cluster_copy(cluster, &K.cta_ovf, sm.cv_ovf);
+    cluster_copy(cluster, &K.cta_pc, sm.cv_i0);
+    cluster_copy(cluster, &K.cta_qc, sm.cv_i1);
+    g.sync();  // the copies, before their readers (the values are not written again here)
     long long bp = 0, bq = 0, ap = 0, aq = 0;
     int op = -1, oq = -1;
     for (unsigned r = 0; r < C; ++r) {
-      bad |= *cluster.map_shared_rank(&K.cta_ovf, r) != 0;
-      const int cp = *cluster.map_shared_rank(&K.cta_pc, r), cq = *cluster.map_shared_rank(&K.cta_qc, r);
+      bad |= sm.cv_ovf[r] != 0;
+      const int cp = sm.cv_i0[r], cq = sm.cv_i1[r];
       if (r == rank) { bp = ap; bq = aq; }
       if (op < 0 && ap < np_cut && np_cut <= ap + cp) op = (int)r;
       if (oq < 0 && aq < nq_cut && nq_cut <= aq + cq) oq = (int)r;
@@ -1113,8 +1233,11 @@ __device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem
       if (qp && oq == (int)rank && lane == 0) K.tie_q = kth_qcut(K, nq_cut - bq);
     }
     cluster.sync();
-    if (pp && op >= 0) tie_p = *cluster.map_shared_rank(&K.tie_p, (unsigned)op);
-    if (qp && oq >= 0) tie_q = *cluster.map_shared_rank(&K.tie_q, (unsigned)oq);
+    if (t == 0 && pp && op >= 0) sm.cv_i0[0] = *cluster.map_shared_rank(&K.tie_p, (unsigned)op);
+    if (t == 1 && qp && oq >= 0) sm.cv_i1[0] = *cluster.map_shared_rank(&K.tie_q, (unsigned)oq);
+    g.sync();
+    if (pp && op >= 0) tie_p = sm.cv_i0[0];
+    if (qp && oq >= 0) tie_q = sm.cv_i1[0];
   }
   // weights of the warp's candidates, and their running sums in id order
   pr.tie = pp ? tie_p : INT_MAX;
@@ -1164,21 +1287,23 @@ __device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem
     sm.cta_ovf = K.cta_ovf;
   }
   cluster.sync();
+  cluster_copy(cluster, &sm.cta_ovf, sm.cv_ovf);
+  cluster_copy(cluster, &sm.cta_sum, sm.cv_sum);
+  cluster.sync();  // every CTA has read the slice totals
   double W = 0.0, acc = 0.0, cbase = 0.0;
   int owner = -1, lastr = -1;
   for (unsigned r = 0; r < C; ++r) {
-    bad |= *cluster.map_shared_rank(&sm.cta_ovf, r) != 0;
-    const double sr = *cluster.map_shared_rank(&sm.cta_sum, r);
+    bad |= sm.cv_ovf[r] != 0;
+    const double sr = sm.cv_sum[r];
     if (sr > 0.0) lastr = (int)r;
     W += sr;
   }
   const double target = u1 * W;
   for (unsigned r = 0; r < C; ++r) {
-    const double sr = *cluster.map_shared_rank(&sm.cta_sum, r);
+    const double sr = sm.cv_sum[r];
     if (sr > 0.0 && acc <= target) { owner = (int)r; cbase = acc; }
     acc += sr;
   }
-  cluster.sync();  // every CTA has read the slice totals
   if (bad) return kNaN64;
   if (!(W > 0.0)) return W;
   if (owner < 0) { owner = lastr; cbase = 0.0; }
