@@ -85,6 +85,11 @@ struct SessSmem {
   long long cv_n0[kMaxCluster], cv_n1[kMaxCluster];
   int cv_ovf[kMaxCluster], cv_i0[kMaxCluster], cv_i1[kMaxCluster];
   long long cv_res;
+  // the draw's target over the cluster, worked out by thread 0 alone (fp64 arithmetic runs at
+  // a small fraction of the fp32 rate on this GPU, so it is kept off the other threads)
+  double d_W, d_target, d_base;
+  float d_tloc;
+  int d_owner, d_bad;
 };
 
 // Lanes r < C of warp 0: dst[r] = the value at src in the shared memory of cluster rank r.
@@ -475,18 +480,20 @@ __device__ int draw_walk(const T* prow, const T* qrow, bool residual, bool al_p,
       const float tv = __shfl_up_sync(0xFFFFFFFFu, incl, o);
       if (lane >= o) incl += tv;
     }
-    // the lanes' intervals tile the segment: lane l covers [carry + incl(l-1), carry +
-    // incl(l)), so a target never falls between two lanes, whatever the rounding of incl
+    // the lanes' intervals tile the segment: lane l covers [incl(l-1), incl(l)) past carry,
+    // so a target never falls between two lanes, whatever the rounding of incl.  The target's
+    // offset past carry is taken once in fp64 and rounded down to a float, dt: for a float x,
+    // x <= dt exactly when x <= target - carry, and dt < x exactly when target - carry < x.
     float ex = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
     if (lane == 0) ex = 0.f;
-    const double start = carry + (double)ex;
+    const float dt = __double2float_rd(target - carry);
     int hit = INT_MAX;
-    if (ls > 0.f && start <= target && target < carry + (double)incl) {
-      double cc = start;
+    if (ls > 0.f && ex <= dt && dt < incl) {
+      float cc = ex;
 #pragma unroll
       for (int e = 0; e < kEpt; ++e) {
-        cc += (double)wv[e];
-        if (hit == INT_MAX && wv[e] > 0.f && cc > target) hit = j0 + e;
+        cc += wv[e];
+        if (hit == INT_MAX && wv[e] > 0.f && cc > dt) hit = j0 + e;
       }
       if (hit == INT_MAX) hit = lp;  // the lane's sum reached the target, its steps fell short
     }
@@ -529,27 +536,30 @@ __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, Se
   cluster_copy(cluster, &sm.tie_q_cand, sm.cv_i1);
   cluster_copy(cluster, &sm.cta_ovf, sm.cv_ovf);
   cluster.sync();  // every CTA has read the slice totals
-  double W = 0.0;
-  int owner = -1, tp_id = INT_MAX, tq_id = INT_MAX, bad = 0;
-  double obase = 0.0;
-  for (unsigned r = 0; r < C; ++r) {
-    W += sm.cv_sum[r];
-    tp_id = min(tp_id, sm.cv_i0[r]);
-    tq_id = min(tq_id, sm.cv_i1[r]);
-    bad |= sm.cv_ovf[r];
-  }
-  const double target = u1 * W;
-  {
+  if (t == 0) {
     // the owner is the last slice with weight whose start is at or below the target (the
     // slices tile [0, W) by construction, whatever the rounding of their sums)
-    double acc = 0.0;
+    double W = 0.0, acc = 0.0, obase = 0.0;
+    int owner = -1, bad = 0;
+    for (unsigned r = 0; r < C; ++r) { W += sm.cv_sum[r]; bad |= sm.cv_ovf[r]; }
+    const double target = u1 * W;
     for (unsigned r = 0; r < C; ++r) {
       const double sr = sm.cv_sum[r];
       if (sr > 0.0 && acc <= target) { owner = (int)r; obase = acc; }
       acc += sr;
     }
+    sm.d_W = W; sm.d_target = target; sm.d_base = obase; sm.d_owner = owner; sm.d_bad = bad;
+    sm.d_tloc = (float)(target - obase);  // the target within the owner's slice
   }
-  if (bad) return kNaN64;
+  g.sync();
+  int tp_id = INT_MAX, tq_id = INT_MAX;
+  for (unsigned r = 0; r < C; ++r) {
+    tp_id = min(tp_id, sm.cv_i0[r]);
+    tq_id = min(tq_id, sm.cv_i1[r]);
+  }
+  const double W = sm.d_W;
+  const int owner = sm.d_owner;
+  if (sm.d_bad) return kNaN64;
   if (!(W > 0.0)) return W;
   if (owner != (int)rank) return W;
   // tie ids found by this pass (the lists); otherwise the caller's stand (found beforehand
@@ -562,7 +572,7 @@ __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, Se
   long long cand = -1;
   float cbase = 0.f;
   {
-    const float tloc = (float)(target - obase);  // the target within this slice
+    const float tloc = sm.d_tloc;  // the target within this slice
     float bsum = pre;
     for (int i = 0; i < gpt; ++i) {
       const int k = t * gpt + i;
@@ -573,11 +583,11 @@ __device__ double locate_and_walk(cg::cluster_group& cluster, const Group& g, Se
     }
   }
   const long long og = group_max_i64(g, cand, sm.lscr);
-  if (og >= 0 && cand == og) sm.owner_base = obase + (double)cbase;
+  if (og >= 0 && cand == og) sm.owner_base = sm.d_base + (double)cbase;
   g.sync();
   if (w == 0 && og >= 0) {
     const int tok = draw_walk<T, FILT, QR>(prow, qrow, residual, al_p, al_q, V, pr, qr, sl.grp_lo((int)og),
-                                       sl.grp_hi((int)og), sm.owner_base, target);
+                                       sl.grp_hi((int)og), sm.owner_base, sm.d_target);
     if (lane == 0) *out = tok;
   }
   return W;
@@ -1290,30 +1300,39 @@ __device__ double draw_kept(cg::cluster_group& cluster, const Group& g, SessSmem
   cluster_copy(cluster, &sm.cta_ovf, sm.cv_ovf);
   cluster_copy(cluster, &sm.cta_sum, sm.cv_sum);
   cluster.sync();  // every CTA has read the slice totals
-  double W = 0.0, acc = 0.0, cbase = 0.0;
-  int owner = -1, lastr = -1;
-  for (unsigned r = 0; r < C; ++r) {
-    bad |= sm.cv_ovf[r] != 0;
-    const double sr = sm.cv_sum[r];
-    if (sr > 0.0) lastr = (int)r;
-    W += sr;
+  if (t == 0) {
+    double W = 0.0, acc = 0.0, cbase = 0.0;
+    int owner = -1, lastr = -1, bd = 0;
+    for (unsigned r = 0; r < C; ++r) {
+      bd |= sm.cv_ovf[r] != 0;
+      const double sr = sm.cv_sum[r];
+      if (sr > 0.0) lastr = (int)r;
+      W += sr;
+    }
+    const double target = u1 * W;
+    for (unsigned r = 0; r < C; ++r) {
+      const double sr = sm.cv_sum[r];
+      if (sr > 0.0 && acc <= target) { owner = (int)r; cbase = acc; }
+      acc += sr;
+    }
+    if (owner < 0) { owner = lastr; cbase = 0.0; }
+    sm.d_W = W; sm.d_target = target; sm.d_base = cbase; sm.d_owner = owner; sm.d_bad = bd;
   }
-  const double target = u1 * W;
-  for (unsigned r = 0; r < C; ++r) {
-    const double sr = sm.cv_sum[r];
-    if (sr > 0.0 && acc <= target) { owner = (int)r; cbase = acc; }
-    acc += sr;
-  }
+  g.sync();
+  bad |= sm.d_bad != 0;
+  const double W = sm.d_W;
   if (bad) return kNaN64;
   if (!(W > 0.0)) return W;
-  if (owner < 0) { owner = lastr; cbase = 0.0; }
-  if (owner != (int)rank) return W;
+  if (sm.d_owner != (int)rank) return W;
   // the owner: the last candidate with weight whose interval starts at or below the target
-  // (a target past every interval, from rounding, takes the last token with weight)
+  // (a target past every interval, from rounding, takes the last token with weight); the
+  // target's offset past the warp's base is rounded down to a float once per warp, so each
+  // candidate's start compares exactly as it would with that offset in fp64
+  const float dt = __double2float_rd(sm.d_target - (sm.d_base + (double)K.wbase[w]));
   int best = -1;
   for (int i = lane; i < nc; i += 32) {
     const float x = K.r[w][i];
-    if (x > 0.f && cbase + (double)K.wbase[w] + (double)K.pre[w][i] <= target) best = i;
+    if (x > 0.f && K.pre[w][i] <= dt) best = i;
   }
   const int wb = __reduce_max_sync(0xFFFFFFFFu, (unsigned)(best + 1)) - 1;
   int anyw = -1;
@@ -1367,7 +1386,8 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
   qr.thr = filt_q ? key_value(sq.thr_key) : -INFINITY;
   pr.tie = INT_MAX;
   qr.tie = INT_MAX;
-  const double u1 = session_uniform(A, b, P, (uint32_t)a, 1u);
+  // the additional token's random value: only thread 0 forms the draw's target from it
+  const double u1 = (threadIdx.x == 0) ? session_uniform(A, b, P, (uint32_t)a, 1u) : 0.0;
   int32_t* out = A.out_tokens + off0 + b + a;
   for (int attempt = 0; attempt < 2; ++attempt) {
     if (QR && residual) {
