@@ -35,25 +35,27 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link libsdcp.so if any source is newer; return its path."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, lib: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile and link libsdcp.so (or, with extra_flags, a variant at `lib` built in
+    `build_dir`) if any source is newer; return its path."""
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmd = [cc] + ARCH + flags + ["-c", src, "-o", obj]
         if verbose:
@@ -69,15 +71,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if failed:
         msg = "\n".join(" ".join(c) + "\n" + o for c, o in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     link = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     if verbose:
         print(" ".join(link), flush=True)
     out = subprocess.run(link, capture_output=True, text=True)
     if out.returncode != 0:
         raise RuntimeError("link failed:\n" + out.stdout + out.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

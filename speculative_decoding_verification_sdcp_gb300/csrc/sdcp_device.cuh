@@ -229,20 +229,23 @@ __device__ __forceinline__ long long warp_sum_ll(long long v) {
   return v;
 }
 
-// Session of a row by a warp-cooperative 32-ary search over m_offsets: the largest b in
+// Session of a row by a warp-cooperative 128-ary search over m_offsets: the largest b in
 // [0, B) with key(b) <= r, key(b) = m_offsets[b] + (target ? b : 0).  Clamped to [0, B).
 __device__ __forceinline__ int32_t find_session(const int32_t* __restrict__ m_offsets, int32_t B,
                                                 int64_t r, bool target) {
   int64_t lo = 0, hi = B;
   const int l = threadIdx.x & 31;
-  while (hi - lo > 1) {
-    const int64_t step = (hi - lo + 31) / 32;
-    const int64_t j = lo + (int64_t)l * step;
-    bool ok = false;
-    if (j < hi) ok = (int64_t)__ldg(&m_offsets[j]) + (target ? j : 0) <= r;
-    const unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
-    const int last = (m == 0) ? 0 : (31 - __clz(m));
-    const int64_t nlo = lo + (int64_t)last * step;
+  while (hi - lo > 1) {  // 128 candidates a round: lane l tests 4 consecutive ones
+    const int64_t step = (hi - lo + 127) / 128;
+    int lastc = -1;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = l * 4 + q;
+      const int64_t j = lo + (int64_t)c * step;
+      if (j < hi && (int64_t)__ldg(&m_offsets[j]) + (target ? j : 0) <= r) lastc = c;
+    }
+    const int best = max(0, (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)(lastc + 1)) - 1);
+    const int64_t nlo = lo + (int64_t)best * step;
     const int64_t nhi = nlo + step;
     lo = nlo;
     hi = nhi < hi ? nhi : hi;
@@ -287,7 +290,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // A waiting thread sleeps until the phase completes or kSuspendNs pass (so a waiting warp
 // takes no issue slots from the warps that work); a wait gives up after kWaitNs in all.
 constexpr uint32_t kSuspendNs = 100000;
+#ifdef SDCP_TEST_WAIT_EXPIRY
+// Test build only (the flag is never set in the library): waits give up after 20 ms, and the
+// row kernel leaves one ring stage unfilled (sdcp_rows.cu), so a wait runs out on purpose.
+constexpr unsigned long long kWaitNs = 20000000ull;
+#else
 constexpr unsigned long long kWaitNs = 2000000000ull;
+#endif
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"

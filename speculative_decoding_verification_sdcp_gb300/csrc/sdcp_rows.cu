@@ -944,10 +944,14 @@ __device__ SlotInfo resolve_row(const RowArgs& A, long long r) {
   if (r >= R_T + io.total) return s;
   const bool is_target = r < R_T;
   const int32_t b = find_session(io.m_offsets, io.B, is_target ? r : r - R_T, is_target);
+  // the draft token is loaded with the session's parameters and offsets (its index needs b
+  // only), and kept when the row turns out to have one
+  const long long tok_guess = is_target ? r - b : r - R_T;
+  const int32_t tok = (tok_guess >= 0 && tok_guess < io.total) ? io.tokens[tok_guess] : -1;
   long long tok_idx = 0;
   s.x = row_ctx(A, r, b, sizeof(T) == 2, s.skip, tok_idx);
   s.row_id = r;
-  s.xt = s.x.has_x ? io.tokens[tok_idx] : -1;
+  s.xt = s.x.has_x ? tok : -1;
   return s;
 }
 
@@ -1015,6 +1019,16 @@ __global__ void __launch_bounds__(kRowThreads, kRowCtasPerSm) row_stats_kernel(R
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
         if (!ok) break;
         const bool first_early = (c == 0) && early;
+#ifdef SDCP_TEST_WAIT_EXPIRY
+        // test build: CTA 0 leaves the stage of its first row's first chunk unfilled (no copy,
+        // no arrival), so its consumers' bounded wait runs out and the call reports
+        // SDCP_S_INTERNAL; the stage is not marked issued, so no drain waits for it
+        if (blockIdx.x == 0 && rcur == 0 && c == 0) {
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (c == nch - 1) { rnext = fetch(); break; }
+          continue;
+        }
+#endif
         if (l == 0) {
           if (first_early && bytes > 0) bulk_copy_g2s(ring + (size_t)stage * kChunk, src, bytes, &sh.full[stage]);
           issued |= 1u << stage;

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libsdcp.so")
 
 SDCP_F32, SDCP_BF16 = 0, 1
 SDCP_RULE_GREEDY, SDCP_RULE_SPECULATIVE_SAMPLING = 1, 2
-S_OK, S_BAD_PROPOSAL, S_LIMIT, S_BAD_PARAMS, S_Q_UNAVAILABLE = 0, 1, 2, 3, 4
+S_OK, S_BAD_PROPOSAL, S_LIMIT, S_BAD_PARAMS, S_Q_UNAVAILABLE, S_INTERNAL = 0, 1, 2, 3, 4, 5
 ROW_INVALID, ROW_X_KEPT, ROW_SKIPPED, ROW_FALLBACK = 1, 2, 4, 8
 MAX_M = 64
 
