@@ -90,6 +90,7 @@ struct SessSmem {
   double d_W, d_target, d_base;
   float d_tloc;
   int d_owner, d_bad;
+  RowStat stash[2];  // the statistics of target row a and draft row a (from the verdict)
 };
 
 // Lanes r < C of warp 0: dst[r] = the value at src in the shared memory of cluster rank r.
@@ -134,9 +135,10 @@ __device__ __forceinline__ RowStat load_stat(const RowStat* p) {
 
 // ---------------------------------------------------------------------------------
 // Verdict (one full warp; every lane returns the same value).  Writes status, accepted,
-// n_out and every output slot except the drawn token.
+// n_out and every output slot except the drawn token, and leaves the statistics of target
+// row a and draft row a in stash[0], stash[1] (the draw's rows; the warp has read them).
 // ---------------------------------------------------------------------------------
-static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write) {
+static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write, RowStat* stash) {
   const int lane = threadIdx.x & 31;
   const sdcp_session_params P = A.params[b];
   const int64_t off0 = A.m_offsets[b], off1 = A.m_offsets[b + 1];
@@ -157,6 +159,7 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
   if (st == SDCP_S_OK && __ldcg(A.error) != 0u) st = SDCP_S_INTERNAL;
   int a = 0;
   int32_t xr[2] = {-1, -1};
+  RowStat kp0{}, kp1{}, kq0{}, kq1{}, sl{};  // this lane's rows (positions lane, lane + 32)
   if (st == SDCP_S_OK) {
     bool range_bad = false, row_bad = false, q_zero = false;
     bool rej[2] = {false, false};
@@ -168,6 +171,7 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
         xr[h] = x;
         if (x < 0 || (int64_t)x >= V) range_bad = true;
         const RowStat sp = load_stat(A.stats + off0 + b + i);
+        if (h == 0) kp0 = sp; else kp1 = sp;
         if (sp.flags & (SDCP_ROW_INVALID | SDCP_ROW_SKIPPED)) row_bad = true;
         if (rule2 && A.q_rows != nullptr) {
           // q as given (Section 5.2 q_rows): q(x) must be a probability, and not zero
@@ -188,6 +192,7 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
           }
         } else if (rule2) {
           const RowStat sq = load_stat(A.stats + R_T + off0 + i);
+          if (h == 0) kq0 = sq; else kq1 = sq;
           if (sq.flags & (SDCP_ROW_INVALID | SDCP_ROW_SKIPPED)) row_bad = true;
           if (!(sq.flags & SDCP_ROW_X_KEPT)) q_zero = true;
           if (tm == 0u) {
@@ -209,7 +214,7 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
       }
     }
     if (lane == 0) {  // the bonus / last target row must be valid too
-      const RowStat sl = load_stat(A.stats + off0 + b + M);
+      sl = load_stat(A.stats + off0 + b + M);
       if (sl.flags & (SDCP_ROW_INVALID | SDCP_ROW_SKIPPED)) row_bad = true;
     }
     if (__any_sync(0xFFFFFFFFu, range_bad)) st = SDCP_S_BAD_PROPOSAL;
@@ -219,6 +224,13 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
     const unsigned r1 = __ballot_sync(0xFFFFFFFFu, rej[1]);
     a = r0 ? (__ffs(r0) - 1) : (r1 ? 32 + __ffs(r1) - 1 : (int)M);
     if (a > M) a = (int)M;
+    // the rows of position a, from the lane that read them
+    const int owner = (a < M) ? (a & 31) : 0;
+    if (lane == owner) {
+      stash[0] = (a == M) ? sl : ((a < 32) ? kp0 : kp1);
+      stash[1] = (a < 32) ? kq0 : kq1;
+    }
+    __syncwarp();
   }
   const bool ok = (st == SDCP_S_OK);
   const bool draw = ok && (rule2 || relaxed) && tm != 0u;
@@ -230,7 +242,7 @@ static __device__ Verdict session_verdict(const SessIO& A, int32_t b, bool write
   if (write && offsets_ok) {
     const int64_t slot0 = off0 + b;
     int32_t extra = -1;
-    if (ok && !draw) extra = load_stat(A.stats + off0 + b + a).argmax;
+    if (ok && !draw) extra = stash[0].argmax;
 #pragma unroll
     for (int h = 0; h < 3; ++h) {
       const int64_t j = lane + 32 * h;
@@ -370,8 +382,10 @@ struct SegSlice {
   int nseg, s0, s1, G, ngrp;
   __device__ __forceinline__ SegSlice(int V, unsigned C, unsigned rank) {
     nseg = (V + kSegIds - 1) / kSegIds;
-    s0 = (int)((long long)nseg * rank / C);
-    s1 = (int)((long long)nseg * (rank + 1) / C);
+    // nseg <= 2^16 (V <= SDCP_MAX_VOCAB) and rank < C <= 8, so the products fit 32 bits (a
+    // 64-bit division is a long emulated sequence on the GPU)
+    s0 = (int)(((unsigned)nseg * rank) / C);
+    s1 = (int)(((unsigned)nseg * (rank + 1u)) / C);
     const int n = s1 - s0;
     G = max(1, (n + kSegCap - 1) / kSegCap);
     ngrp = (n + G - 1) / G;
@@ -1369,8 +1383,8 @@ __device__ void session_draw(const SessIO& A, cg::cluster_group& cluster, const 
   const T* drow = !residual ? reinterpret_cast<const T*>(A.target) + (off0 + b + a) * (int64_t)V
                   : QR ? reinterpret_cast<const T*>(A.q_rows + (off0 + a) * (int64_t)V)
                        : reinterpret_cast<const T*>(A.draft) + (off0 + a) * (int64_t)V;
-  const RowStat sp = load_stat(A.stats + off0 + b + a);
-  const RowStat sq = (residual && !QR) ? load_stat(A.stats + R_T + off0 + a) : sp;
+  const RowStat sp = sm.stash[0];  // target row a and draft row a, left by the verdict
+  const RowStat sq = (residual && !QR) ? sm.stash[1] : sp;
   const float c = profile_c(P.temperature_milli);
   const bool al_p = ((uintptr_t)trow & 15u) == 0, al_q = ((uintptr_t)drow & 15u) == 0;
   const unsigned C = cluster.num_blocks(), rank = cluster.block_rank();
@@ -1450,7 +1464,7 @@ template <typename T, bool QR = false>
 __device__ void complete_session(const SessIO& A, cg::cluster_group& cluster, const Group& g,
                                               SessSmem& sm, unsigned char* ring, int32_t b) {
   if ((threadIdx.x >> 5) == 0) {
-    const Verdict v = session_verdict(A, b, cluster.block_rank() == 0);
+    const Verdict v = session_verdict(A, b, cluster.block_rank() == 0, sm.stash);
     if ((threadIdx.x & 31) == 0) { sm.st = v.st; sm.a = v.a; sm.draw = v.draw ? 1 : 0; }
   }
   g.sync();
