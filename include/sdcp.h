@@ -222,7 +222,7 @@ int sdcp_row_stats(const void* target_logits, const void* draft_logits, int dtyp
 /*
  * sdcp_verify_batch for callers that cannot allocate device memory.
  *
- * The paper has no counterpart to this entry point: it exists for callers that must not
+ * The SDCP draft has no counterpart to this entry point: it exists for callers that must not
  * call cudaMalloc, such as code running inside a CUDA graph being built by someone else,
  * an allocator-less runtime, or a plugin whose host forbids device allocations.  Instead
  * of a caller-provided workspace it uses a scratch array of SDCP_NOALLOC_SCRATCH_BYTES that
